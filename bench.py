@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark: one decode step of weight-absorbed MLA over a paged latent cache.
+
+A step is the whole hot path on one batch: the split-KV planner
+(mla_decode_plan), the main attention kernel and the split merge
+(mla_decode), on synthetic inputs already resident in HBM.  The default
+workload is the 4K-uniform decode batch (B=64, s_q=1, 128 heads, every
+seq_len 4096); ``--workload`` picks another for manual runs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line.  ``value`` is KV-cache TB/s (algorithmic bytes: every
+cached row once, 1152 B per key) over all ranks; TFLOPS, microseconds per
+step and the roofline fraction ride along.  ``--impl reference`` times the
+fp64 CPU oracle on a bounded sample of the same workload instead.
+
+Multi-GPU runs are replicas (the path shards by request with no exchange):
+launch with torchrun, one rank per GPU, each rank running the full workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "MLA decode KV-cache TB/s, TFLOPS and % of GB300 roofline; µs per decode step"
+NORTH_STAR_HBM_TBS = 8.0
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MAIN_KERNEL_SRC = os.path.join(ROOT, "mla_decode_attention_02_gb300", "csrc")
+
+
+def _args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for ~3 s of timed work)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(MAIN_KERNEL_SRC)):
+        if name.startswith("mla_main") or name.endswith((".h", ".cuh")):
+            with open(os.path.join(MAIN_KERNEL_SRC, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload: str):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != _kernel_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_baseline(w, inp, budget_s: float = 15.0):
+    """The oracle as it stands, on this host's cores, over a bounded sample of the workload."""
+    import oracle
+    threads = oracle.default_threads()
+
+    def run(reqs):
+        rows = [(b, t, h) for b in reqs for t in range(w.s_q) for h in range(W.NUM_HEADS)]
+        t0 = time.perf_counter()
+        oracle.decode(inp["q_latent"], inp["q_rope"], inp["kv_cache"], inp["block_table"],
+                      inp["seq_lens"], s_q=w.s_q, scale=inp["scale"], rows=rows, threads=threads)
+        return time.perf_counter() - t0
+
+    order = sorted(range(w.batch), key=lambda b: w.seq_lens[b])
+    # calibrate on the shortest request, then grow the sample to the time budget
+    t1 = run([order[0]])
+    per_key = t1 / max(1, w.seq_lens[order[0]])
+    reqs, keys = [], 0
+    for b in order:
+        if (keys + w.seq_lens[b]) * per_key > budget_s and reqs:
+            break
+        reqs.append(b)
+        keys += w.seq_lens[b]
+    dt = run(reqs)
+    nbytes = W.cache_bytes([w.seq_lens[b] for b in reqs])
+    return {"value": nbytes / dt / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(reqs)} of {w.batch} requests (all {W.NUM_HEADS} heads, "
+                      f"{keys} keys), {dt:.1f} s wall, fp64"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return 0
+    import oracle
+    w = W.workload(args.workload)
+    inp = W.make_inputs(w)
+    threads = oracle.default_threads()
+    b = min(range(w.batch), key=lambda i: w.seq_lens[i])
+    # rows of one request per step; cap heads so a step stays around a second
+    heads = W.NUM_HEADS
+    rows_all = [(b, t, h) for t in range(w.s_q) for h in range(heads)]
+    t0 = time.perf_counter()
+    oracle.decode(inp["q_latent"], inp["q_rope"], inp["kv_cache"], inp["block_table"],
+                  inp["seq_lens"], s_q=w.s_q, scale=inp["scale"], rows=rows_all[:8],
+                  threads=threads)
+    per_row = (time.perf_counter() - t0) / 8
+    nrows = max(threads, min(len(rows_all), int(1.0 / max(per_row, 1e-9))))
+    rows = rows_all[:nrows]
+    steps = args.steps if args.steps is not None else 20
+    times = []
+    for i in range(args.warmup + steps):
+        t0 = time.perf_counter()
+        oracle.decode(inp["q_latent"], inp["q_rope"], inp["kv_cache"], inp["block_table"],
+                      inp["seq_lens"], s_q=w.s_q, scale=inp["scale"], rows=rows, threads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    frac = nrows / (w.s_q * W.NUM_HEADS)
+    nbytes = W.cache_bytes([w.seq_lens[b]]) * frac
+    value = nbytes / dt / 1e12
+    sample = (f"request {b} (seq_len {w.seq_lens[b]}), {nrows} of {w.s_q * W.NUM_HEADS} "
+              f"(token, head) rows per step, fp64 oracle")
+    line = {"metric": METRIC, "value": value, "unit": "TB/s", "impl": "reference",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(w),
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    lens = sorted(set(w.seq_lens))
+    desc = (f"{w.batch}x{lens[0]}" if len(lens) == 1 else
+            f"{len(w.seq_lens)} rows, seq_len {min(lens)}..{max(lens)}")
+    return {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "heads": W.NUM_HEADS,
+            "d_latent": W.D_LATENT, "d_rope": W.D_ROPE, "page": W.PAGE, "seq_lens": desc,
+            "total_keys": sum(w.seq_lens),
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write); "
+                  f"cache {W.cache_bytes(w.seq_lens) / 1e6:.0f} MB"}
+
+
+def run_native(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import mla_decode_attention_02_gb300 as mla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = W.workload(args.workload)
+    cpu = W.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    B, S = w.batch, w.s_q
+    mp = d["block_table"].shape[1]
+    ws = torch.empty(mla.workspace_size(B, S, mp), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, S, W.NUM_HEADS, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, S, W.NUM_HEADS), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        p = mla.plan(d["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
+        mla.decode(p, d["q_latent"], d["q_rope"], d["kv_cache"], d["block_table"],
+                   scale=d["scale"], out=out, lse=lse, events=events)
+        return p
+
+    for _ in range(max(3, args.warmup)):
+        p = step()
+    status = mla.check(p)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} during warm-up")
+
+    steps = args.steps
+    if steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            flush.fill_(1)
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / 5 / 1e3
+        steps = int(min(20000, max(20, 3.0 / max(per, 1e-6))))
+        if world > 1:
+            t = torch.tensor([steps], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MIN)
+            steps = int(t.item())
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev_s = [mk() for _ in range(steps)]
+    ev_e = [mk() for _ in range(steps)]
+    ev_k = [[mk(), mk(), mk()] for _ in range(steps)]
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = time.time()
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        ev_s[k].record(stream)
+        step(events=ev_k[k])
+        ev_e[k].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_end = time.time()
+    clocks = sampler.summary(t_start, t_end) if sampler else None
+
+    step_ms = statistics.mean(ev_s[k].elapsed_time(ev_e[k]) for k in range(steps))
+    main_ms = statistics.mean(ev_k[k][0].elapsed_time(ev_k[k][1]) for k in range(steps))
+    comb_ms = statistics.mean(ev_k[k][1].elapsed_time(ev_k[k][2]) for k in range(steps))
+    plan_ms = statistics.mean(ev_s[k].elapsed_time(ev_k[k][0]) for k in range(steps))
+    if world > 1:
+        t = torch.tensor([step_ms, main_ms, comb_ms, plan_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, main_ms, comb_ms, plan_ms = t.tolist()
+
+    cache_b = W.cache_bytes(w.seq_lens)
+    fl = W.flops(w.seq_lens, S)
+    value = world * cache_b / (step_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, step, result -> host
+    e2e = None
+    if not args.no_e2e:
+        names = ["q_latent", "q_rope", "block_table", "seq_lens"]
+        host = {k: cpu[k].pin_memory() for k in names}
+        dbuf = {k: torch.empty_like(d[k]) for k in names}
+        o_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        l_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+        d2h = o_host.numel() * o_host.element_size() + l_host.numel() * l_host.element_size()
+        k_e2e = min(steps, 200)
+
+        def e2e_step():
+            for k in names:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            p = mla.plan(dbuf["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
+            mla.decode(p, dbuf["q_latent"], dbuf["q_rope"], d["kv_cache"], dbuf["block_table"],
+                       scale=d["scale"], out=out, lse=lse)
+            o_host.copy_(out, non_blocking=True)
+            l_host.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [mk() for _ in range(k_e2e)]
+        ee = [mk() for _ in range(k_e2e)]
+        for k in range(k_e2e):
+            flush.fill_(k & 0xFF)
+            es[k].record(stream)
+            e2e_step()
+            ee[k].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = statistics.mean(es[k].elapsed_time(ee[k]) for k in range(k_e2e))
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = t.item()
+        e2e = {"value": world * cache_b / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": k_e2e,
+               "note": "per-step inputs (q_latent, q_rope, block_table, seq_lens) copied from "
+                       "pinned host memory and o_latent + lse read back each step; the KV cache "
+                       "is device-resident serving state"}
+
+    status = mla.check(p)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+
+    peaks, peak_src = _peaks()
+    hbm_peak = peaks["hbm_gbs"]
+    main_gbs = cache_b / (main_ms * 1e-3) / 1e9
+    main_tflops = fl / (main_ms * 1e-3) / 1e12
+    hbm_frac = main_gbs / hbm_peak
+    tensor_frac = main_tflops / peaks["bf16_tflops"]
+    bound = "hbm" if hbm_frac >= tensor_frac else "tensor"
+    roof = {"kernel": "mla_decode_main", "bound": bound,
+            "achieved": main_gbs if bound == "hbm" else main_tflops,
+            "peak": hbm_peak if bound == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": hbm_frac if bound == "hbm" else tensor_frac,
+            "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": cache_b, "flops_per_launch": fl,
+            "launch_ms": main_ms, "hbm_frac": hbm_frac, "tensor_frac": tensor_frac}
+    t_roof = max(cache_b / (NORTH_STAR_HBM_TBS * 1e12), fl / (peaks["bf16_tflops"] * 1e12))
+    t_roof_meas = max(cache_b / (hbm_peak * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_base = _cpu_baseline(w, cpu)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": step_ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": _config(w),
+                "tflops": world * fl / (step_ms * 1e-3) / 1e12,
+                "us_per_step": step_ms * 1e3,
+                "phases_us": {"plan": plan_ms * 1e3, "main": main_ms * 1e3,
+                              "combine": comb_ms * 1e3},
+                "roofline_frac_8tbs": t_roof / (step_ms * 1e-3),
+                "roofline_frac_measured_peaks": t_roof_meas / (step_ms * 1e-3),
+                "e2e": e2e, "gpu_launches": 3 * steps, "roofline": roof,
+                "cpu_baseline": cpu_base, "clocks": clocks,
+                "device": torch.cuda.get_device_name(dev), "units": mla.num_units()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = _args()
+    rank, world, local = _dist()
+    if world != args.gpus and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_native(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

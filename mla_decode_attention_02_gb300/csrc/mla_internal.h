@@ -1,0 +1,137 @@
+// Internal definitions shared by the library's CUDA sources: the workspace
+// layout of the split-KV schedule and the planner's per-row arithmetic,
+// which the device planner and its host twin both run so that their output
+// is bit-identical.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mla_decode.h"
+
+#if defined(__CUDACC__)
+#define MLA_HD __host__ __device__ __forceinline__
+#else
+#define MLA_HD inline
+#endif
+
+namespace mla {
+
+constexpr int kHeads = MLA_NUM_HEADS;    // query heads sharing one latent row
+constexpr int kDl = MLA_D_LATENT;        // c_kv values per cached row (also V)
+constexpr int kDr = MLA_D_ROPE;          // k_rope values per cached row
+constexpr int kDrow = kDl + kDr;         // 576 values per cached row
+constexpr int kPage = MLA_PAGE_SIZE;     // tokens per cache page
+constexpr uint32_t kPlanMagic = 0x31414c4du;  // "MLA1"
+
+// Planner tuning, in units of one cache page of work: the fixed cost of a
+// work item (query load, pipeline fill, epilogue) and the shortest split.
+constexpr int kItemCost = 4;
+constexpr int kMinSplitPages = 8;
+
+struct PlanHeader {  // 64 bytes at workspace offset 0
+    uint32_t magic;
+    int32_t batch, s_q, max_pages;
+    int32_t num_units, num_rows, max_items, num_items;
+    int32_t num_parts, status, item_cost, min_split;
+    int64_t total_cost, target;
+};
+static_assert(sizeof(PlanHeader) == 64, "header layout");
+
+// One contiguous key range of one (request, query token) row.
+struct WorkItem {
+    int32_t row;       // b * s_q + t
+    int32_t kv_begin;  // first key (a multiple of the page size)
+    int32_t kv_end;    // one past the last key
+    int32_t part;      // partial slot, or -1: this item is the whole row
+};
+static_assert(sizeof(WorkItem) == 16, "item layout");
+
+// Byte offsets of every region of the workspace.
+struct PlanLayout {
+    size_t items, item_unit, unit_begin, row_nparts, row_part0, row_item0, row_pos, plan_end;
+    size_t lse_part, o_part, total;
+    int32_t num_rows, max_items, max_parts;
+};
+
+MLA_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+MLA_HD PlanLayout plan_layout(int32_t batch, int32_t s_q, int32_t num_units) {
+    PlanLayout L;
+    L.num_rows = batch * s_q;
+    L.max_items = L.num_rows + num_units;
+    L.max_parts = L.max_items;
+    size_t off = sizeof(PlanHeader);
+    L.items = off;
+    off += sizeof(WorkItem) * (size_t)L.max_items;
+    L.item_unit = off;
+    off += sizeof(int32_t) * (size_t)L.max_items;
+    L.unit_begin = off;
+    off += sizeof(int32_t) * ((size_t)num_units + 1);
+    L.row_nparts = off;
+    off += sizeof(int32_t) * (size_t)L.num_rows;
+    L.row_part0 = off;
+    off += sizeof(int32_t) * (size_t)L.num_rows;
+    L.row_item0 = off;
+    off += sizeof(int32_t) * (size_t)L.num_rows;
+    off = align_up(off, 8);
+    L.row_pos = off;
+    off += sizeof(int64_t) * (size_t)L.num_rows;
+    L.plan_end = off;
+    off = align_up(off, 256);
+    L.lse_part = off;
+    off += sizeof(float) * (size_t)L.max_parts * kHeads;
+    off = align_up(off, 256);
+    L.o_part = off;
+    off += sizeof(float) * (size_t)L.max_parts * kHeads * kDl;
+    L.total = align_up(off, 256);
+    return L;
+}
+
+// Pages row r = (b, t) must read, or -1 when its seq_len is invalid.
+MLA_HD int32_t row_pages(int32_t seq_len, int32_t s_q, int32_t t, int32_t max_pages) {
+    int64_t vis = (int64_t)seq_len - s_q + 1 + t;
+    if (seq_len < s_q || vis < 1) return -1;
+    int64_t pages = (vis + kPage - 1) / kPage;
+    if (seq_len > (int64_t)max_pages * kPage) return -1;
+    return (int32_t)pages;
+}
+
+MLA_HD int64_t row_cost(int32_t pages) { return pages > 0 ? (int64_t)pages + kItemCost : 0; }
+
+// Walks the unit boundaries that fall inside one row's stretch of the cost
+// line [x0, x0 + cost) and cuts the row there, except where a piece would
+// be shorter than kMinSplitPages: a short leading piece moves to the next
+// unit, a short trailing piece stays with the previous one.  Calls
+// emit(piece, first_page, end_page, unit) for every piece and returns the
+// number of pieces.
+#if defined(__CUDACC__)
+#pragma nv_exec_check_disable
+#endif
+template <typename Emit>
+MLA_HD int32_t cut_row(int64_t x0, int32_t pages, int64_t target, int32_t num_units, Emit emit) {
+    if (pages <= 0) return 0;
+    const int64_t cost = row_cost(pages);
+    int64_t unit = x0 / target;
+    int64_t start = 0;
+    int32_t n = 0;
+    for (int64_t k = unit + 1; k * target < x0 + cost && k < num_units; ++k) {
+        int64_t cut = k * target - x0 - kItemCost;
+        if (cut - start >= kMinSplitPages && pages - cut >= kMinSplitPages) {
+            emit(n, (int32_t)start, (int32_t)cut, (int32_t)unit);
+            ++n;
+            start = cut;
+            unit = k;
+        } else if (cut - start < kMinSplitPages) {
+            unit = k;
+        }
+    }
+    emit(n, (int32_t)start, pages, (int32_t)unit);
+    return n + 1;
+}
+
+struct NoEmit {
+    MLA_HD void operator()(int32_t, int32_t, int32_t, int32_t) const {}
+};
+
+}  // namespace mla
