@@ -62,6 +62,40 @@ def _dist():
     return rank, world, local
 
 
+_CUDART = None
+
+
+def _event_ms(e0, e1) -> float:
+    """cudaEventElapsedTime on torch events that the library recorded through the C ABI.
+
+    torch only reports elapsed time for events it recorded itself, so this asks the
+    CUDA runtime that torch already loaded.
+    """
+    import ctypes
+    global _CUDART
+    if _CUDART is None:
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                _CUDART = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if _CUDART is None:
+            import glob
+            import torch
+            cands = glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*",
+                                           "lib", "libcudart.so*"))
+            _CUDART = ctypes.CDLL(cands[0])
+        _CUDART.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+    ms = ctypes.c_float(0.0)
+    rc = _CUDART.cudaEventElapsedTime(ctypes.byref(ms), ctypes.c_void_p(e0.cuda_event),
+                                      ctypes.c_void_p(e1.cuda_event))
+    if rc != 0:
+        raise RuntimeError(f"cudaEventElapsedTime failed ({rc})")
+    return ms.value
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -290,6 +324,10 @@ def run_native(args, rank, world, local):
     ev_s = [mk() for _ in range(steps)]
     ev_e = [mk() for _ in range(steps)]
     ev_k = [[mk(), mk(), mk()] for _ in range(steps)]
+    for evs in ev_k:          # torch creates the CUDA event on first record; the library
+        for e in evs:         # re-records these through the C ABI inside the timed loop
+            e.record(stream)
+    torch.cuda.synchronize()
 
     gpu_id = None
     try:
@@ -313,10 +351,10 @@ def run_native(args, rank, world, local):
     t_end = time.time()
     clocks = sampler.summary(t_start, t_end) if sampler else None
 
-    step_ms = statistics.mean(ev_s[k].elapsed_time(ev_e[k]) for k in range(steps))
-    main_ms = statistics.mean(ev_k[k][0].elapsed_time(ev_k[k][1]) for k in range(steps))
-    comb_ms = statistics.mean(ev_k[k][1].elapsed_time(ev_k[k][2]) for k in range(steps))
-    plan_ms = statistics.mean(ev_s[k].elapsed_time(ev_k[k][0]) for k in range(steps))
+    step_ms = statistics.mean(_event_ms(ev_s[k], ev_e[k]) for k in range(steps))
+    main_ms = statistics.mean(_event_ms(ev_k[k][0], ev_k[k][1]) for k in range(steps))
+    comb_ms = statistics.mean(_event_ms(ev_k[k][1], ev_k[k][2]) for k in range(steps))
+    plan_ms = statistics.mean(_event_ms(ev_s[k], ev_k[k][0]) for k in range(steps))
     if world > 1:
         t = torch.tensor([step_ms, main_ms, comb_ms, plan_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
