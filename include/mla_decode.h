@@ -171,6 +171,40 @@ size_t mla_decode_plan_bytes(const mla_problem *prob, int32_t num_units);
 mla_status mla_decode_plan_host(const mla_problem *prob, const int32_t *seq_lens_host,
                                 int32_t num_units, void *plan_host, size_t plan_bytes);
 
+/*
+ * Allocation-free variant of plan + decode.  The pages have no counterpart
+ * of this entry point: it exists for callers that cannot call cudaMalloc on
+ * their decode path, such as serving loops and plugin hosts that own every
+ * byte of device memory, or latency-critical code where an allocation (which
+ * may synchronise the device and has unbounded latency) is forbidden.
+ *
+ * It runs mla_decode_plan and mla_decode with the workspace placed in a
+ * file-scope static device array of MLA_NOALLOC_SCRATCH_BYTES bytes inside
+ * the library, so the caller passes only inputs and outputs (same layouts
+ * and meanings as mla_decode; seq_lens is a device pointer).  Every GPU on
+ * which this entry point runs holds that array until the process exits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Problems whose workspace (mla_decode_workspace_size) exceeds
+ *    MLA_NOALLOC_SCRATCH_BYTES are rejected with MLA_ERR_WORKSPACE before
+ *    anything is enqueued.
+ *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *    routine is called.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    every call rewrites the schedule and status word before reading them.
+ *    Calls that overlap on the GPU (e.g. on two streams, or from two host
+ *    threads without ordering) race on the array and give wrong results:
+ *    order them on one stream.
+ *  - The device status word is not readable through mla_decode_check here;
+ *    rows with device-detected input errors are still written as NaN.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+mla_status mla_decode_noalloc(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                              const void *kv_cache, int64_t num_pages, const int32_t *block_table,
+                              const int32_t *seq_lens, float scale, void *o_latent, float *lse,
+                              mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

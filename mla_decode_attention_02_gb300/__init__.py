@@ -11,10 +11,12 @@ ctypes binding with the same names:
 
 from ._binding import (DEFAULT_SCALE, D_LATENT, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
                        MLA_DEV_BAD_PAGE, MLA_DEV_BAD_PLAN, MLA_DEV_BAD_SEQ_LEN, MLA_DEV_TIMEOUT,
-                       MLAError, Plan, check, decode, load_library, num_units, parse_plan, plan,
+                       MLAError, NOALLOC_SCRATCH_BYTES, Plan, check, decode, decode_noalloc,
+                       load_library, num_units, parse_plan, plan,
                        plan_device_bytes, plan_host, plan_layout, workspace_size)
 
 __all__ = ["DEFAULT_SCALE", "D_LATENT", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
            "MLA_DEV_BAD_PAGE", "MLA_DEV_BAD_PLAN", "MLA_DEV_BAD_SEQ_LEN", "MLA_DEV_TIMEOUT",
-           "MLAError", "Plan", "check", "decode", "load_library", "num_units", "parse_plan",
+           "MLAError", "NOALLOC_SCRATCH_BYTES", "Plan", "check", "decode", "decode_noalloc",
+           "load_library", "num_units", "parse_plan",
            "plan", "plan_device_bytes", "plan_host", "plan_layout", "workspace_size"]

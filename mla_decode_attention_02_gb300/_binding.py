@@ -56,6 +56,8 @@ _SIGS = {
                                   _vp, _vp, ctypes.c_size_t, _vp]),
     "mla_decode_timed": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_float,
                                         _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
+    "mla_decode_noalloc": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
+                                          ctypes.c_float, _vp, _vp, _vp]),
     "mla_decode_check": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mla_decode_plan_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
@@ -203,6 +205,44 @@ def decode(p: Plan, q_latent, q_rope, kv_cache, block_table, *, scale: float = D
             handles = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) if e is not None
                                               else None for e in events])
             _check(load_library().mla_decode_timed(*args, handles), "mla_decode_timed")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def decode_noalloc(q_latent, q_rope, kv_cache, block_table, seq_lens, *, s_q: int,
+                   scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None):
+    """Plan + decode through ``mla_decode_noalloc``: the library allocates nothing.
+
+    For callers that cannot allocate device memory on their decode path; the
+    workspace lives in a fixed 64 MiB device array inside the library, shared
+    by every call (order calls on one stream).  Problems needing a larger
+    workspace raise MLAError (status 3).  out / lse may be passed in so that
+    this call allocates nothing on the Python side either.
+    """
+    import torch
+    _req(seq_lens, "seq_lens", torch.int32, None, None)
+    dev = seq_lens.device
+    B = seq_lens.shape[0]
+    _req(q_latent, "q_latent", torch.bfloat16, (B, s_q, NUM_HEADS, D_LATENT), dev)
+    _req(q_rope, "q_rope", torch.bfloat16, (B, s_q, NUM_HEADS, D_ROPE), dev)
+    _req(kv_cache, "kv_cache", torch.bfloat16, None, dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch][max_pages_per_seq]")
+    _req(block_table, "block_table", torch.int32, None, dev)
+    if out is None:
+        out = torch.empty((B, s_q, NUM_HEADS, D_LATENT), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, NUM_HEADS), dtype=torch.float32, device=dev)
+    _req(out, "out", torch.bfloat16, (B, s_q, NUM_HEADS, D_LATENT), dev)
+    _req(lse, "lse", torch.float32, (B, s_q, NUM_HEADS), dev)
+    prob = _problem(B, s_q, block_table.shape[1])
+    with torch.cuda.device(dev):
+        _check(load_library().mla_decode_noalloc(
+            ctypes.byref(prob), q_latent.data_ptr(), q_rope.data_ptr(), kv_cache.data_ptr(),
+            kv_cache.shape[0], block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
+            out.data_ptr(), lse.data_ptr(), _stream_handle(stream)), "mla_decode_noalloc")
     return out, lse
 
 
