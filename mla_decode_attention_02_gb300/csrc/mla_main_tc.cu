@@ -1,0 +1,697 @@
+// Main attention kernel: weight-absorbed MLA decode on the 5th-generation
+// tensor cores (tcgen05 + TMEM), pages streamed by TMA.
+//
+// What it computes is the attention of "Huawei Ascend servers: DeepSeek
+// V3/R1 inference best practice" §3.2.1 (128 heads share one 576-value
+// cached row per token, weights absorbed) as tiled exact softmax attention
+// (§6.1, after FlashAttention), over the key ranges the split-KV schedule
+// hands each work unit (FlashDecoding, Atlas 800I A3 troubleshooting post).
+//
+// GB300 design.  The fp32 output of one row is 128 heads x 512 values =
+// 256 KB, all of one SM's tensor memory, so a work unit is a cluster of two
+// CTAs on two SMs that split the cache row between them:
+//
+//   CTA c holds latent dims [256c, 256c + 256) and rope dims [32c, 32c + 32)
+//   of q (72 KB in shared memory for the whole work item) and TMA-loads the
+//   same 288 values of every cached token (36 KB per 64-token page), so the
+//   cluster reads each cached byte from HBM exactly once.
+//
+//   S_c = q_c . k_c^T     tcgen05 M=128 (heads) N=64 (tokens) K=288, fp32 in TMEM
+//   S   = S_0 + S_1       each CTA sends its partial to the peer through
+//                          distributed shared memory (st.async), and both add
+//                          the two partials: the same sum in both CTAs, so the
+//                          softmax below is bit-identical on both sides
+//   P   = exp2(S*scale*log2e - m)     fp32 online softmax, lazily rescaled,
+//                          rounded to bf16 into TMEM
+//   O_c += P . V_c        tcgen05 M=128 N=256 K=64, A = P from TMEM,
+//                          B = the page's latent dims [256c, 256c+256)
+//
+// Each CTA keeps its 256 output columns in TMEM (plus two S and two P
+// buffers: 448 of 512 columns).  Warp roles per CTA: warp 0 issues TMA,
+// warp 1 owns TMEM and issues the MMAs, warps 2-5 (one thread per head) do
+// the softmax, the exchange and the epilogue.  Every wait is bounded: on
+// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
+// hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kStages = 3;          // KV page ring
+constexpr int kClusterSize = 2;
+constexpr uint32_t kQLatBlk = 128 * 128;           // q block: 128 heads x 64 dims (SW128)
+constexpr uint32_t kQBytes = 4 * kQLatBlk + 128 * 64;  // + rope 128 x 32 dims (SW64)
+constexpr uint32_t kKvLatBlk = 64 * 128;           // page block: 64 tokens x 64 dims
+constexpr uint32_t kStageBytes = 4 * kKvLatBlk + 64 * 64;  // + rope 64 x 32 dims
+constexpr uint32_t kXRow = 272;                    // exchange row: 64 fp32 + 16 B pad
+constexpr uint32_t kXBytes = 128 * kXRow;
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffStage = kQBytes;            // 73728, 1024-aligned
+constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
+constexpr uint32_t kOffBar = kOffX + kXBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "TMA/UMMA tile alignment");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// TMEM columns
+constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
+constexpr uint32_t kColS = 256;     // 2 x 64 fp32 score buffers
+constexpr uint32_t kColP = 384;     // 2 x 32 columns of packed bf16 probabilities
+constexpr uint32_t kTmemCols = 512;
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
+
+// barrier slots (8 bytes each) in the barrier area
+enum : uint32_t {
+    B_Q_FULL = 0,
+    B_Q_EMPTY = 1,
+    B_KV_FULL = 2,                  // + stage
+    B_KV_EMPTY = B_KV_FULL + kStages,
+    B_S_FULL = B_KV_EMPTY + kStages,  // + buffer
+    B_S_EMPTY = B_S_FULL + 2,
+    B_P_FULL = B_S_EMPTY + 2,
+    B_PV_DONE = B_P_FULL + 2,
+    B_X_FULL = B_PV_DONE + 2,
+    B_X_FREE = B_X_FULL + 1,
+    B_O_FREE = B_X_FREE + 1,
+    B_DRAIN = B_O_FREE + 1,
+    B_COUNT = B_DRAIN + 1,
+};
+static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
+
+struct Params {
+    CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
+    CUtensorMap tm_q_rope;  // q_rope   as [rows*128][64],  box 32 x 128, SW64
+    CUtensorMap tm_kv_lat;  // kv_cache as [pages][64][576], box 64 x 64 x 1, SW128
+    CUtensorMap tm_kv_rope; // kv_cache,                     box 32 x 64 x 1, SW64
+    const int32_t *block_table;
+    uint8_t *ws;
+    __nv_bfloat16 *o_latent;
+    float *lse;
+    int64_t num_pages;
+    float scale_log2;
+    int32_t batch, s_q, max_pages, num_units;
+};
+
+struct Ctl {
+    uint32_t bar0;       // shared address of barrier 0
+    volatile int *abort; // shared abort flag
+    int *status;         // device status word
+};
+
+__device__ __forceinline__ uint32_t bar(const Ctl &c, uint32_t i) { return c.bar0 + 8u * i; }
+
+__device__ __forceinline__ void fail(const Ctl &c) {
+    if (!*c.abort) {
+        *c.abort = 1;
+        atomicOr(c.status, MLA_DEV_TIMEOUT);
+    }
+}
+
+// Bounded wait for the completion of the phase with the given parity: gives
+// up (and flags the time-out) after kWaitLimitNs, or at once if another
+// thread of the CTA already gave up.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_impl(const Ctl &c, uint32_t b, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
+        if ((i & 255) == 255) {
+            if (*c.abort) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitLimitNs) {
+                fail(c);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity) {
+    return wait_impl<false>(c, b, parity);
+}
+
+__device__ __forceinline__ bool wait_cluster(const Ctl &c, uint32_t b, uint32_t parity) {
+    return wait_impl<true>(c, b, parity);
+}
+
+// Warp-uniform versions: every lane waits (and acquires), and the warp agrees
+// on the outcome, so no lane leaves a .sync.aligned sequence early.
+__device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait(c, b, parity));
+}
+
+__device__ __forceinline__ bool wait_cluster_warp(const Ctl &c, uint32_t b, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_cluster(c, b, parity));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+mla_main_tc_kernel(const __grid_constant__ Params P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t s_q = s_base + kOffQ;
+    const uint32_t s_stage = s_base + kOffStage;
+    uint8_t *x_buf = smem + kOffX;
+    const uint32_t s_x = s_base + kOffX;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t unit = cluster_id_x();
+
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(P.ws);
+    Ctl ctl;
+    ctl.bar0 = s_base + kOffBar;
+    ctl.abort = &abort_flag;
+    ctl.status = &hdr->status;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(bar(ctl, B_Q_FULL), 1);
+        mbar_init(bar(ctl, B_Q_EMPTY), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(ctl, B_KV_FULL + s), 1);
+            mbar_init(bar(ctl, B_KV_EMPTY + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(ctl, B_S_FULL + i), 1);
+            mbar_init(bar(ctl, B_S_EMPTY + i), 4);
+            mbar_init(bar(ctl, B_P_FULL + i), 4);
+            mbar_init(bar(ctl, B_PV_DONE + i), 1);
+        }
+        mbar_init(bar(ctl, B_X_FULL), 128);
+        mbar_init(bar(ctl, B_X_FREE), 4);
+        mbar_init(bar(ctl, B_O_FREE), 4);
+        mbar_init(bar(ctl, B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&P.tm_q_lat);
+        prefetch_tmap(&P.tm_q_rope);
+        prefetch_tmap(&P.tm_kv_lat);
+        prefetch_tmap(&P.tm_kv_rope);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // peer barriers are initialised before any remote access
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    const PlanLayout L = plan_layout(P.batch, P.s_q, P.num_units);
+    const WorkItem *items = reinterpret_cast<const WorkItem *>(P.ws + L.items);
+    const int32_t *unit_begin = reinterpret_cast<const int32_t *>(P.ws + L.unit_begin);
+    float *lse_part = reinterpret_cast<float *>(P.ws + L.lse_part);
+    float *o_part = reinterpret_cast<float *>(P.ws + L.o_part);
+    const bool plan_ok = hdr->magic == kPlanMagic && hdr->batch == P.batch &&
+                         hdr->s_q == P.s_q && hdr->num_units == P.num_units &&
+                         hdr->max_pages == P.max_pages && (int)unit < P.num_units;
+    int i_begin = 0, i_end = 0;
+    if (plan_ok) {
+        i_begin = unit_begin[unit];
+        i_end = unit_begin[unit + 1];
+    } else if (threadIdx.x == 0 && rank == 0) {
+        atomicOr(&hdr->status, MLA_DEV_BAD_PLAN);
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t g = 0;
+        for (int i = i_begin; i < i_end && !abort_flag; ++i) {
+            const WorkItem it = items[i];
+            const int b = it.row / P.s_q;
+            const int p0 = it.kv_begin / kPage;
+            const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+            const uint32_t ii = (uint32_t)(i - i_begin);
+            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
+            if (lane == 0) {
+                const uint32_t fb = bar(ctl, B_Q_FULL);
+                mbar_arrive_expect_tx(fb, kQBytes);
+                const int y = it.row * kHeads;
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_load_2d(s_q + kb * kQLatBlk, &P.tm_q_lat, (int)rank * 256 + kb * 64, y, fb);
+                tma_load_2d(s_q + 4 * kQLatBlk, &P.tm_q_rope, (int)rank * 32, y, fb);
+            }
+            for (int k0 = 0; k0 < n && !abort_flag; k0 += 32) {
+                const int mine = k0 + lane < n
+                                     ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane]
+                                     : 0;
+                const int cnt = min(32, n - k0);
+                for (int kk = 0; kk < cnt; ++kk, ++g) {
+                    const int page = __shfl_sync(0xffffffffu, mine, kk);
+                    const uint32_t s = g % kStages;
+                    if (g >= kStages &&
+                        !wait_warp(ctl, bar(ctl, B_KV_EMPTY + s), ((g / kStages) - 1) & 1))
+                        break;
+                    if (lane == 0) {
+                        const uint32_t fb = bar(ctl, B_KV_FULL + s);
+                        const uint32_t dst = s_stage + s * kStageBytes;
+                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        // An out-of-pool page index reads zeros (TMA bounds fill);
+                        // the softmax warps flag the row.
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_load_3d(dst + kb * kKvLatBlk, &P.tm_kv_lat,
+                                        (int)rank * 256 + kb * 64, 0, page, fb);
+                        tma_load_3d(dst + 4 * kKvLatBlk, &P.tm_kv_rope, 512 + (int)rank * 32, 0,
+                                    page, fb);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+            uint32_t g = 0;
+            auto issue_pv = [&](uint32_t gg, bool first, uint32_t ii) -> bool {
+                const uint32_t pb = gg & 1;
+                if (!wait(ctl, bar(ctl, B_P_FULL + pb), (gg >> 1) & 1)) return false;
+                if (first && ii > 0 && !wait(ctl, bar(ctl, B_O_FREE), (ii - 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t v = s_stage + (gg % kStages) * kStageBytes;
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bdesc = smem_desc(v + ks * 2048, 8192, 1024, 2);
+                    mma_ts(tmem + kColO, tmem + kColP + pb * 32 + ks * 8, bdesc, id_pv,
+                           (first && ks == 0) ? 0u : 1u);
+                }
+                mma_commit(bar(ctl, B_PV_DONE + pb));
+                mma_commit(bar(ctl, B_KV_EMPTY + gg % kStages));
+                return true;
+            };
+            bool ok = true;
+            for (int i = i_begin; i < i_end && ok; ++i) {
+                const WorkItem it = items[i];
+                const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+                const uint32_t ii = (uint32_t)(i - i_begin);
+                if (!wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+                for (int k = 0; k < n && ok; ++k, ++g) {
+                    const uint32_t s = g % kStages, sb = g & 1;
+                    if (!wait(ctl, bar(ctl, B_KV_FULL + s), (g / kStages) & 1)) { ok = false; break; }
+                    if (g >= 2 && !wait(ctl, bar(ctl, B_S_EMPTY + sb), ((g >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kv = s_stage + s * kStageBytes;
+                    const uint32_t d = tmem + kColS + sb * 64;
+                    uint32_t acc = 0;
+                    for (int kb = 0; kb < 4; ++kb)
+                        for (int ks = 0; ks < 4; ++ks) {
+                            mma_ss(d, smem_desc(s_q + kb * kQLatBlk + ks * 32, 16, 1024, 2),
+                                   smem_desc(kv + kb * kKvLatBlk + ks * 32, 16, 1024, 2), id_qk,
+                                   acc);
+                            acc = 1;
+                        }
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_ss(d, smem_desc(s_q + 4 * kQLatBlk + ks * 32, 16, 512, 4),
+                               smem_desc(kv + 4 * kKvLatBlk + ks * 32, 16, 512, 4), id_qk, 1);
+                    mma_commit(bar(ctl, B_S_FULL + sb));
+                    if (k == n - 1) mma_commit(bar(ctl, B_Q_EMPTY));
+                    if (k >= 1) ok = issue_pv(g - 1, k == 1, ii);
+                }
+                if (ok) ok = issue_pv(g - 1, n == 1, ii);
+            }
+            // wind down: every MMA this thread issued completes before TMEM is freed
+            mma_commit(bar(ctl, B_DRAIN));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(ctl, B_DRAIN), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+        const int h = quarter * 32 + lane;         // head = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + kColS;
+        const uint32_t tP = tmem + lane_off + kColP;
+        const uint32_t tO = tmem + lane_off + kColO;
+        const uint32_t my_x = s_x + h * kXRow;
+        const uint32_t peer_x = mapa(my_x, peer);
+        const uint32_t peer_x_full = mapa(bar(ctl, B_X_FULL), peer);
+        const uint32_t peer_x_free = mapa(bar(ctl, B_X_FREE), peer);
+        const float NEG_INF = -INFINITY;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const WorkItem it = items[i];
+            const int b = it.row / P.s_q;
+            const int p0 = it.kv_begin / kPage;
+            const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+            const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
+            const uint32_t ii = (uint32_t)(i - i_begin);
+            // every page of the item must lie in the pool
+            bool bad = false;
+            for (int k0 = 0; k0 < n; k0 += 32) {
+                int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
+                bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
+            }
+            float m_run = NEG_INF, l_run = 0.f;
+            for (int k = 0; k < n; ++k, ++g) {
+                const uint32_t sb = g & 1;
+                if (!wait_warp(ctl, bar(ctl, B_S_FULL + sb), (g >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tS + sb * 64, r0);
+                tmem_ld32(tS + sb * 64 + 32, r1);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY + sb));
+
+                // exchange partial scores with the peer CTA
+                if (g >= 1 && !wait_cluster_warp(ctl, bar(ctl, B_X_FREE), (g - 1) & 1)) { ok = false; break; }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_async_v4(peer_x + q * 16, __uint_as_float(r0[4 * q]),
+                                __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
+                                __uint_as_float(r0[4 * q + 3]), peer_x_full);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_async_v4(peer_x + 128 + q * 16, __uint_as_float(r1[4 * q]),
+                                __uint_as_float(r1[4 * q + 1]), __uint_as_float(r1[4 * q + 2]),
+                                __uint_as_float(r1[4 * q + 3]), peer_x_full);
+                mbar_arrive_expect_tx(bar(ctl, B_X_FULL), 256);
+                if (!wait_cluster_warp(ctl, bar(ctl, B_X_FULL), g & 1)) { ok = false; break; }
+                float s[64];
+                const float4 *xr = reinterpret_cast<const float4 *>(x_buf + h * kXRow);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 v = xr[q];
+                    s[4 * q] = v.x;
+                    s[4 * q + 1] = v.y;
+                    s[4 * q + 2] = v.z;
+                    s[4 * q + 3] = v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(peer_x_free);
+
+                // full scores (own + peer: the same sum on both CTAs), masked tail
+                const int valid = (k == n - 1) ? valid_last : kPage;
+                float m_loc = NEG_INF;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float a = (__uint_as_float(r0[j]) + s[j]) * P.scale_log2;
+                    float c = (__uint_as_float(r1[j]) + s[32 + j]) * P.scale_log2;
+                    a = j < valid ? a : NEG_INF;
+                    c = 32 + j < valid ? c : NEG_INF;
+                    s[j] = a;
+                    s[32 + j] = c;
+                    m_loc = fmaxf(m_loc, fmaxf(a, c));
+                }
+                // lazy rescale of the running output
+                float alpha = 1.f;
+                bool need = false;
+                if (k == 0) {
+                    m_run = m_loc;
+                } else if (m_loc > m_run + kRescaleThreshold) {
+                    alpha = fast_exp2(m_run - m_loc);
+                    m_run = m_loc;
+                    need = true;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    if (!wait_warp(ctl, bar(ctl, B_PV_DONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + ch * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(tO + ch * 32, o);
+                    }
+                    tmem_wait_st();
+                    l_run *= alpha;
+                }
+                // probabilities -> bf16 -> TMEM
+                uint32_t pk[32];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float e0 = fast_exp2(s[2 * j] - m_run);
+                    const float e1 = fast_exp2(s[2 * j + 1] - m_run);
+                    lsum += e0 + e1;
+                    pk[j] = pack_bf16(e0, e1);
+                }
+                l_run += lsum;
+                if (g >= 2 && !wait_warp(ctl, bar(ctl, B_PV_DONE + sb), ((g - 2) >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(tP + sb * 32, pk);
+                tmem_wait_st();
+                if (valid < kPage) {
+                    // zero the latent rows of the masked tail so that 0 * garbage stays 0
+                    uint8_t *stage = smem + kOffStage + (g % kStages) * kStageBytes;
+                    const int nchunk = (kPage - valid) * 4 * 8;  // 16-byte chunks
+                    for (int idx = (warp - 2) * 32 + lane; idx < nchunk; idx += 128) {
+                        const int blk = idx / ((kPage - valid) * 8);
+                        const int rem = idx % ((kPage - valid) * 8);
+                        const int tok = valid + rem / 8;
+                        *reinterpret_cast<uint4 *>(stage + blk * kKvLatBlk + tok * 128 +
+                                                   (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_P_FULL + sb));
+            }
+            if (!ok) break;
+
+            // epilogue: wait for the last PV, normalise, store this CTA's half
+            if (!wait_warp(ctl, bar(ctl, B_PV_DONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1)) break;
+            tc_fence_after();
+            const float nan = __int_as_float(0x7fc00000);
+            const float inv = bad ? nan : 1.f / l_run;
+            const float lse = bad ? nan : (m_run + log2f(l_run)) * 0.69314718055994531f;
+            const size_t hrow = (size_t)it.row * kHeads + h;
+            if (it.part < 0) {
+                uint4 *dst = reinterpret_cast<uint4 *>(P.o_latent + hrow * kDl + rank * 256);
+#pragma unroll 1
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                        v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                        v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                        v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                        dst[ch * 4 + q] = v;
+                    }
+                }
+                if (rank == 0) P.lse[hrow] = lse;
+            } else {
+                const size_t slot = (size_t)it.part * kHeads + h;
+                float4 *dst = reinterpret_cast<float4 *>(o_part + slot * kDl + rank * 256);
+#pragma unroll 1
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[ch * 8 + q] = make_float4(__uint_as_float(o[4 * q]) * inv,
+                                                      __uint_as_float(o[4 * q + 1]) * inv,
+                                                      __uint_as_float(o[4 * q + 2]) * inv,
+                                                      __uint_as_float(o[4 * q + 3]) * inv);
+                }
+                if (rank == 0) lse_part[slot] = lse;
+            }
+            if (bad && lane == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
+            (void)ii;
+        }
+    }
+
+    // teardown: both CTAs finish (no remote access in flight) before TMEM is freed
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int units = 0;
+    bool attr_set = false;
+};
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+cudaError_t prepare(int dev, int *units) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(mla_main_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kClusterSize * (sms / kClusterSize));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = kClusterSize;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, mla_main_tc_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        d.units = n;
+        d.attr_set = true;
+    }
+    *units = d.units;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t main_units(int32_t *units) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int u = 0;
+    e = prepare(dev, &u);
+    if (e != cudaSuccess) return e;
+    *units = u;
+    return cudaSuccess;
+}
+
+cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv,
+                        int64_t num_pages, const int32_t *block_table, float scale, void *ws,
+                        void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
+                        int32_t num_units, cudaStream_t stream) {
+    Params p;
+    const cuuint64_t qrows = (cuuint64_t)batch * s_q * kHeads;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kDl, qrows};
+        cuuint64_t strides[1] = {(cuuint64_t)kDl * 2};
+        cuuint32_t box[2] = {64, 128};
+        if (!encode(&p.tm_q_lat, q_latent, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kDr, qrows};
+        cuuint64_t strides[1] = {(cuuint64_t)kDr * 2};
+        cuuint32_t box[2] = {32, 128};
+        if (!encode(&p.tm_q_rope, q_rope, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)kDrow, (cuuint64_t)kPage, (cuuint64_t)num_pages};
+        cuuint64_t strides[2] = {(cuuint64_t)kDrow * 2, (cuuint64_t)kDrow * 2 * kPage};
+        cuuint32_t box_lat[3] = {64, 64, 1};
+        cuuint32_t box_rope[3] = {32, 64, 1};
+        if (!encode(&p.tm_kv_lat, kv, 3, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&p.tm_kv_rope, kv, 3, dims, strides, box_rope, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    }
+    p.block_table = block_table;
+    p.ws = static_cast<uint8_t *>(ws);
+    p.o_latent = static_cast<__nv_bfloat16 *>(o_latent);
+    p.lse = lse;
+    p.num_pages = num_pages;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.batch = batch;
+    p.s_q = s_q;
+    p.max_pages = max_pages;
+    p.num_units = num_units;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterSize * num_units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kClusterSize;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_main_tc_kernel, p);
+}
+
+}  // namespace mla
