@@ -7,7 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/mla_decode.h"
+#include "mla_decode.h"
 
 #if defined(__CUDACC__)
 #define MLA_HD __host__ __device__ __forceinline__

@@ -2,36 +2,36 @@
 // tensor cores (tcgen05 + TMEM), pages streamed by TMA.
 //
 // What it computes is the attention of "Huawei Ascend servers: DeepSeek
-// V3/R1 inference best practice" §3.2.1 (128 heads share one 576-value
-// cached row per token, weights absorbed) as tiled exact softmax attention
-// (§6.1, after FlashAttention), over the key ranges the split-KV schedule
-// hands each work unit (FlashDecoding, Atlas 800I A3 troubleshooting post).
+// V3/R1 inference best practice" section 3.2.1 (128 heads share one
+// 576-value cached row per token, weights absorbed) as tiled exact softmax
+// attention (section 6.1, after FlashAttention), over the key ranges the
+// split-KV schedule hands each work unit (FlashDecoding, Atlas 800I A3
+// troubleshooting post).
 //
-// GB300 design.  The fp32 output of one row is 128 heads x 512 values =
-// 256 KB, all of one SM's tensor memory, so a work unit is a cluster of two
-// CTAs on two SMs that split the cache row between them:
+// GB300 design.  The fp32 output of one row (128 heads x 512 values =
+// 256 KB) alone fills one SM's tensor memory, so a work unit is a cluster of
+// two CTAs on two SMs, and CTA c owns output columns [256c, 256c + 256).
+// Cross-SM traffic through distributed shared memory measures only
+// 10-20 GB/s per SM on this part, far too slow to exchange per-page score
+// partials, so nothing is exchanged per page: each CTA computes the full
+// score tile itself and the pair shares only the page loads.
 //
-//   CTA c holds latent dims [256c, 256c + 256) and rope dims [32c, 32c + 32)
-//   of q (72 KB in shared memory for the whole work item) and TMA-loads the
-//   same 288 values of every cached token (36 KB per 64-token page), so the
-//   cluster reads each cached byte from HBM exactly once.
+//   page g (64 tokens x 576) -> TMA multicast: CTA 0 loads dim blocks 0-4,
+//                               CTA 1 blocks 5-8, each into both CTAs
+//   S   = q . k^T            tcgen05 M=128 (heads) N=64 (tokens) K=576, fp32
+//                            in TMEM; q dims 0-319 are the A operand in TMEM,
+//                            dims 320-575 in shared memory
+//   P   = exp2(S*scale*log2e - m)    fp32 online softmax with a lazily
+//                            raised running max, rounded to bf16 into TMEM
+//   O_c += P . V_c           tcgen05 M=128 N=256 K=64, A = P from TMEM,
+//                            B = the page's latent dims [256c, 256c + 256)
 //
-//   S_c = q_c . k_c^T     tcgen05 M=128 (heads) N=64 (tokens) K=288, fp32 in TMEM
-//   S   = S_0 + S_1       each CTA sends its partial to the peer through
-//                          distributed shared memory (st.async), and both add
-//                          the two partials: the same sum in both CTAs, so the
-//                          softmax below is bit-identical on both sides
-//   P   = exp2(S*scale*log2e - m)     fp32 online softmax, lazily rescaled,
-//                          rounded to bf16 into TMEM
-//   O_c += P . V_c        tcgen05 M=128 N=256 K=64, A = P from TMEM,
-//                          B = the page's latent dims [256c, 256c+256)
-//
-// Each CTA keeps its 256 output columns in TMEM (plus two S and two P
-// buffers: 448 of 512 columns).  Warp roles per CTA: warp 0 issues TMA,
-// warp 1 owns TMEM and issues the MMAs, warps 2-5 (one thread per head) do
-// the softmax, the exchange and the epilogue.  Every wait is bounded: on
-// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
-// hanging.
+// TMEM (512 columns): O half [0,256), S [256,320), P [320,352), q [352,512).
+// Warp roles per CTA: warp 0 issues TMA, warp 1 owns TMEM and issues the QK
+// MMAs, warp 6 issues the PV MMAs (one thread issues a tcgen05.mma about
+// every 27 ns, so the two chains get their own issuers), warps 2-5 (one
+// thread per head) load q into TMEM and run the softmax and the epilogue.  Every wait is bounded: on time-out the kernel
+// records MLA_DEV_TIMEOUT and winds down instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,55 +47,56 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
-constexpr int kStages = 3;          // KV page ring
+constexpr int kThreads = 224;       // warp 0 TMA, warp 1 QK MMA, warps 2-5 softmax, warp 6 PV MMA
+constexpr int kPvWarp = 6;
+constexpr int kStages = 2;          // KV page ring (a full page per stage)
+constexpr int kPrefetch = 4;        // pages requested into L2 ahead of their stage load
 constexpr int kClusterSize = 2;
-constexpr uint32_t kQLatBlk = 128 * 128;           // q block: 128 heads x 64 dims (SW128)
-constexpr uint32_t kQBytes = 4 * kQLatBlk + 128 * 64;  // + rope 128 x 32 dims (SW64)
-constexpr uint32_t kKvLatBlk = 64 * 128;           // page block: 64 tokens x 64 dims
-constexpr uint32_t kStageBytes = 4 * kKvLatBlk + 64 * 64;  // + rope 64 x 32 dims
-constexpr uint32_t kXRow = 272;                    // exchange row: 64 fp32 + 16 B pad
-constexpr uint32_t kXBytes = 128 * kXRow;
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffStage = kQBytes;            // 73728, 1024-aligned
-constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffX + kXBytes;
+constexpr uint16_t kBoth = 0x3;     // multicast mask: both CTAs of the pair
+constexpr uint32_t kBlk = 64 * 128;               // page block: 64 tokens x 64 dims (SW128)
+constexpr uint32_t kStageBytes = 9 * kBlk;        // dims 0-511 latent + 512-575 rope
+constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims (SW128)
+constexpr uint32_t kQSBytes = 4 * kQBlk;          // q dims 320-575 in shared memory
+constexpr int kQTDims = 320;                      // q dims 0-319 live in TMEM
+constexpr uint32_t kOffQS = 0;
+constexpr uint32_t kOffStage = kQSBytes;
+constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers, + alignment slack
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
-constexpr uint32_t kColS = 256;     // 2 x 64 fp32 score buffers
-constexpr uint32_t kColP = 384;     // 2 x 32 columns of packed bf16 probabilities
+constexpr uint32_t kColS = 256;     // 64 fp32 scores
+constexpr uint32_t kColP = 320;     // 32 columns of packed bf16 probabilities
+constexpr uint32_t kColQ = 352;     // 160 columns of packed bf16 q (dims 0-319)
 constexpr uint32_t kTmemCols = 512;
+static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,
-    B_Q_EMPTY = 1,
+    B_Q_FULL = 0,                   // producer (+tx) and 4 softmax warps (q in TMEM)
+    B_Q_EMPTY = 1,                  // last QK of an item done, in both CTAs
     B_KV_FULL = 2,                  // + stage
-    B_KV_EMPTY = B_KV_FULL + kStages,
-    B_S_FULL = B_KV_EMPTY + kStages,  // + buffer
-    B_S_EMPTY = B_S_FULL + 2,
-    B_P_FULL = B_S_EMPTY + 2,
-    B_PV_DONE = B_P_FULL + 2,
-    B_X_FULL = B_PV_DONE + 2,
-    B_X_FREE = B_X_FULL + 1,
-    B_O_FREE = B_X_FREE + 1,
-    B_DRAIN = B_O_FREE + 1,
-    B_COUNT = B_DRAIN + 1,
+    B_KV_EMPTY = B_KV_FULL + kStages,  // + stage; both CTAs' PVs done
+    B_S_FULL = B_KV_EMPTY + kStages,
+    B_S_EMPTY = B_S_FULL + 1,
+    B_P_FULL = B_S_EMPTY + 1,
+    B_PV_DONE = B_P_FULL + 1,
+    B_O_FREE = B_PV_DONE + 1,
+    B_DRAIN = B_O_FREE + 1,         // + issuer (0: QK, 1: PV)
+    B_COUNT = B_DRAIN + 2,
 };
 static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
 
 struct Params {
     CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
-    CUtensorMap tm_q_rope;  // q_rope   as [rows*128][64],  box 32 x 128, SW64
-    CUtensorMap tm_kv_lat;  // kv_cache as [pages][64][576], box 64 x 64 x 1, SW128
-    CUtensorMap tm_kv_rope; // kv_cache,                     box 32 x 64 x 1, SW64
+    CUtensorMap tm_q_rope;  // q_rope   as [rows*128][64],  box 64 x 128, SW128
+    CUtensorMap tm_kv;      // kv_cache as [pages][64][576], box 64 x 64 x 1, SW128
+    const __nv_bfloat16 *q_latent;
     const int32_t *block_table;
     uint8_t *ws;
     __nv_bfloat16 *o_latent;
@@ -123,11 +124,10 @@ __device__ __forceinline__ void fail(const Ctl &c) {
 // Bounded wait for the completion of the phase with the given parity: gives
 // up (and flags the time-out) after kWaitLimitNs, or at once if another
 // thread of the CTA already gave up.
-template <bool kCluster>
-__device__ __forceinline__ bool wait_impl(const Ctl &c, uint32_t b, uint32_t parity) {
+__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
-        if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
+        if (mbar_try_wait(b, parity)) return true;
         if ((i & 255) == 255) {
             if (*c.abort) return false;
             const uint64_t t = globaltimer_ns();
@@ -141,22 +141,10 @@ __device__ __forceinline__ bool wait_impl(const Ctl &c, uint32_t b, uint32_t par
     }
 }
 
-__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity) {
-    return wait_impl<false>(c, b, parity);
-}
-
-__device__ __forceinline__ bool wait_cluster(const Ctl &c, uint32_t b, uint32_t parity) {
-    return wait_impl<true>(c, b, parity);
-}
-
-// Warp-uniform versions: every lane waits (and acquires), and the warp agrees
+// Warp-uniform version: every lane waits (and acquires), and the warp agrees
 // on the outcome, so no lane leaves a .sync.aligned sequence early.
 __device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity) {
     return __all_sync(0xffffffffu, wait(c, b, parity));
-}
-
-__device__ __forceinline__ bool wait_cluster_warp(const Ctl &c, uint32_t b, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait_cluster(c, b, parity));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -176,16 +164,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t s_q = s_base + kOffQ;
+    const uint32_t s_qs = s_base + kOffQS;
     const uint32_t s_stage = s_base + kOffStage;
-    uint8_t *x_buf = smem + kOffX;
-    const uint32_t s_x = s_base + kOffX;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const uint32_t peer = rank ^ 1u;
     const uint32_t unit = cluster_id_x();
 
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(P.ws);
@@ -196,29 +181,25 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(ctl, B_Q_FULL), 1);
-        mbar_init(bar(ctl, B_Q_EMPTY), 1);
+        mbar_init(bar(ctl, B_Q_FULL), 5);
+        mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(ctl, B_KV_FULL + s), 1);
-            mbar_init(bar(ctl, B_KV_EMPTY + s), 1);
+            mbar_init(bar(ctl, B_KV_EMPTY + s), kClusterSize);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(ctl, B_S_FULL + i), 1);
-            mbar_init(bar(ctl, B_S_EMPTY + i), 4);
-            mbar_init(bar(ctl, B_P_FULL + i), 4);
-            mbar_init(bar(ctl, B_PV_DONE + i), 1);
-        }
-        mbar_init(bar(ctl, B_X_FULL), 128);
-        mbar_init(bar(ctl, B_X_FREE), 4);
+        mbar_init(bar(ctl, B_S_FULL), 1);
+        mbar_init(bar(ctl, B_S_EMPTY), 4);
+        mbar_init(bar(ctl, B_P_FULL), 4);
+        mbar_init(bar(ctl, B_PV_DONE), 1);
         mbar_init(bar(ctl, B_O_FREE), 4);
         mbar_init(bar(ctl, B_DRAIN), 1);
+        mbar_init(bar(ctl, B_DRAIN + 1), 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&P.tm_q_lat);
         prefetch_tmap(&P.tm_q_rope);
-        prefetch_tmap(&P.tm_kv_lat);
-        prefetch_tmap(&P.tm_kv_rope);
+        prefetch_tmap(&P.tm_kv);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
@@ -226,7 +207,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // peer barriers are initialised before any remote access
+    cluster_sync();  // the peer's barriers are initialised before any multicast targets them
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
@@ -255,100 +236,120 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
+            // q dims 320-575: both CTAs' copies must be free (last QK of the previous item)
             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
             if (lane == 0) {
                 const uint32_t fb = bar(ctl, B_Q_FULL);
-                mbar_arrive_expect_tx(fb, kQBytes);
+                mbar_arrive_expect_tx(fb, kQSBytes);
                 const int y = it.row * kHeads;
-                for (int kb = 0; kb < 4; ++kb)
-                    tma_load_2d(s_q + kb * kQLatBlk, &P.tm_q_lat, (int)rank * 256 + kb * 64, y, fb);
-                tma_load_2d(s_q + 4 * kQLatBlk, &P.tm_q_rope, (int)rank * 32, y, fb);
+                for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j) {
+                    if (j < 3)
+                        tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_lat, kQTDims + 64 * j, y, fb, kBoth);
+                    else
+                        tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                }
             }
-            for (int k0 = 0; k0 < n && !abort_flag; k0 += 32) {
-                const int mine = k0 + lane < n
-                                     ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane]
-                                     : 0;
+            bool ok = true;
+            const int kb0 = rank == 0 ? 0 : 5, kb1 = rank == 0 ? 5 : 9;  // this CTA's blocks
+            const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
+            // pages [0, kPrefetch) of the item go to L2 at once
+            if (lane < min(kPrefetch, n)) {
+                const int pg = bt[lane];
+                for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, pg);
+            }
+            for (int k0 = 0; k0 < n && ok; k0 += 32) {
+                const int mine = k0 + lane < n ? bt[k0 + lane] : 0;
+                const int ahead = k0 + lane + kPrefetch < n ? bt[k0 + lane + kPrefetch] : 0;
                 const int cnt = min(32, n - k0);
                 for (int kk = 0; kk < cnt; ++kk, ++g) {
                     const int page = __shfl_sync(0xffffffffu, mine, kk);
+                    const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
                     const uint32_t s = g % kStages;
+                    if (lane == 0 && k0 + kk + kPrefetch < n)
+                        for (int kb = kb0; kb < kb1; ++kb)
+                            tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, page_ahead);
+                    // the stage is free in both CTAs (our loads write into both)
                     if (g >= kStages &&
-                        !wait_warp(ctl, bar(ctl, B_KV_EMPTY + s), ((g / kStages) - 1) & 1))
+                        !wait_warp(ctl, bar(ctl, B_KV_EMPTY + s), ((g / kStages) - 1) & 1)) {
+                        ok = false;
                         break;
+                    }
                     if (lane == 0) {
                         const uint32_t fb = bar(ctl, B_KV_FULL + s);
                         const uint32_t dst = s_stage + s * kStageBytes;
                         mbar_arrive_expect_tx(fb, kStageBytes);
                         // An out-of-pool page index reads zeros (TMA bounds fill);
                         // the softmax warps flag the row.
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_load_3d(dst + kb * kKvLatBlk, &P.tm_kv_lat,
-                                        (int)rank * 256 + kb * 64, 0, page, fb);
-                        tma_load_3d(dst + 4 * kKvLatBlk, &P.tm_kv_rope, 512 + (int)rank * 32, 0,
-                                    page, fb);
+                        for (int kb = kb0; kb < kb1; ++kb)
+                            tma_load_3d_mc(dst + kb * kBlk, &P.tm_kv, 64 * kb, 0, page, fb, kBoth);
                     }
                     __syncwarp();
                 }
             }
+            if (!ok) break;
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
-            const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+            const bool qk_role = warp == 1;
+            // Descriptor bases; every MMA below adds a compile-time byte offset (>> 4).
+            const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
+            const uint64_t d_kv0 = smem_desc(s_stage, 16, 1024, 2);
+            const uint64_t d_v0 = smem_desc(s_stage + 4 * rank * kBlk, 8192, 1024, 2);
+            constexpr uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+            const uint32_t tS = tmem + kColS, tQ = tmem + kColQ, tO = tmem + kColO, tP = tmem + kColP;
             uint32_t g = 0;
-            auto issue_pv = [&](uint32_t gg, bool first, uint32_t ii) -> bool {
-                const uint32_t pb = gg & 1;
-                if (!wait(ctl, bar(ctl, B_P_FULL + pb), (gg >> 1) & 1)) return false;
-                if (first && ii > 0 && !wait(ctl, bar(ctl, B_O_FREE), (ii - 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t v = s_stage + (gg % kStages) * kStageBytes;
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bdesc = smem_desc(v + ks * 2048, 8192, 1024, 2);
-                    mma_ts(tmem + kColO, tmem + kColP + pb * 32 + ks * 8, bdesc, id_pv,
-                           (first && ks == 0) ? 0u : 1u);
-                }
-                mma_commit(bar(ctl, B_PV_DONE + pb));
-                mma_commit(bar(ctl, B_KV_EMPTY + gg % kStages));
-                return true;
-            };
             bool ok = true;
             for (int i = i_begin; i < i_end && ok; ++i) {
                 const WorkItem it = items[i];
                 const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
                 const uint32_t ii = (uint32_t)(i - i_begin);
-                if (!wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+                if (qk_role && !wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
                 for (int k = 0; k < n && ok; ++k, ++g) {
-                    const uint32_t s = g % kStages, sb = g & 1;
-                    if (!wait(ctl, bar(ctl, B_KV_FULL + s), (g / kStages) & 1)) { ok = false; break; }
-                    if (g >= 2 && !wait(ctl, bar(ctl, B_S_EMPTY + sb), ((g >> 1) - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kv = s_stage + s * kStageBytes;
-                    const uint32_t d = tmem + kColS + sb * 64;
-                    uint32_t acc = 0;
-                    for (int kb = 0; kb < 4; ++kb)
-                        for (int ks = 0; ks < 4; ++ks) {
-                            mma_ss(d, smem_desc(s_q + kb * kQLatBlk + ks * 32, 16, 1024, 2),
-                                   smem_desc(kv + kb * kKvLatBlk + ks * 32, 16, 1024, 2), id_qk,
-                                   acc);
-                            acc = 1;
+                    const uint32_t s = g % kStages;
+                    const uint64_t stage_off = (uint64_t)((s * kStageBytes) >> 4);
+                    if (qk_role) {
+                        // S = q . k^T over all 576 dims
+                        if (!wait(ctl, bar(ctl, B_KV_FULL + s), (g / kStages) & 1)) { ok = false; break; }
+                        if (g >= 1 && !wait(ctl, bar(ctl, B_S_EMPTY), (g - 1) & 1)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t kv = d_kv0 + stage_off;
+#pragma unroll
+                        for (int ks = 0; ks < kQTDims / 16; ++ks)  // q from TMEM, dims 0-319
+                            mma_ts(tS, tQ + 8 * ks,
+                                   kv + (uint64_t)(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4), id_qk,
+                                   ks > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)               // q from smem, dims 320-575
+                            mma_ss(tS, d_qs + (uint64_t)(((j >> 2) * kQBlk + (j & 3) * 32) >> 4),
+                                   kv + (uint64_t)(((5 + (j >> 2)) * kBlk + (j & 3) * 32) >> 4),
+                                   id_qk, 1u);
+                        mma_commit(bar(ctl, B_S_FULL));
+                        if (k == n - 1) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
+                    } else {
+                        // O_c (+)= P . V_c
+                        if (!wait(ctl, bar(ctl, B_P_FULL), g & 1)) { ok = false; break; }
+                        if (k == 0 && ii > 0 && !wait(ctl, bar(ctl, B_O_FREE), (ii - 1) & 1)) {
+                            ok = false;
+                            break;
                         }
-                    for (int ks = 0; ks < 2; ++ks)
-                        mma_ss(d, smem_desc(s_q + 4 * kQLatBlk + ks * 32, 16, 512, 4),
-                               smem_desc(kv + 4 * kKvLatBlk + ks * 32, 16, 512, 4), id_qk, 1);
-                    mma_commit(bar(ctl, B_S_FULL + sb));
-                    if (k == n - 1) mma_commit(bar(ctl, B_Q_EMPTY));
-                    if (k >= 1) ok = issue_pv(g - 1, k == 1, ii);
+                        tc_fence_after();
+                        const uint64_t v = d_v0 + stage_off;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ts(tO, tP + ks * 8, v + (uint64_t)((ks * 2048) >> 4), id_pv,
+                                   (k == 0 && ks == 0) ? 0u : 1u);
+                        mma_commit(bar(ctl, B_PV_DONE));
+                        mma_commit_mc(bar(ctl, B_KV_EMPTY + s), kBoth);
+                    }
                 }
-                if (ok) ok = issue_pv(g - 1, n == 1, ii);
             }
             // wind down: every MMA this thread issued completes before TMEM is freed
-            mma_commit(bar(ctl, B_DRAIN));
+            const uint32_t drain = bar(ctl, B_DRAIN + (qk_role ? 0 : 1));
+            mma_commit(drain);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(ctl, B_DRAIN), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
         }
         __syncwarp();
@@ -360,10 +361,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const uint32_t tS = tmem + lane_off + kColS;
         const uint32_t tP = tmem + lane_off + kColP;
         const uint32_t tO = tmem + lane_off + kColO;
-        const uint32_t my_x = s_x + h * kXRow;
-        const uint32_t peer_x = mapa(my_x, peer);
-        const uint32_t peer_x_full = mapa(bar(ctl, B_X_FULL), peer);
-        const uint32_t peer_x_free = mapa(bar(ctl, B_X_FREE), peer);
+        const uint32_t tQ = tmem + lane_off + kColQ;
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
         bool ok = true;
@@ -374,6 +372,30 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
+
+            // q dims 0-319 of this head -> TMEM (the A operand of the first 20 k-steps)
+            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    P.q_latent + ((size_t)it.row * kHeads + h) * kDl);
+#pragma unroll 1
+                for (int c = 0; c < 5; ++c) {
+                    uint32_t q[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 x = src[c * 8 + v];
+                        q[4 * v] = x.x;
+                        q[4 * v + 1] = x.y;
+                        q[4 * v + 2] = x.z;
+                        q[4 * v + 3] = x.w;
+                    }
+                    tmem_st32(tQ + c * 32, q);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
+            }
             // every page of the item must lie in the pool
             bool bad = false;
             for (int k0 = 0; k0 < n; k0 += 32) {
@@ -382,51 +404,23 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
             float m_run = NEG_INF, l_run = 0.f;
             for (int k = 0; k < n; ++k, ++g) {
-                const uint32_t sb = g & 1;
-                if (!wait_warp(ctl, bar(ctl, B_S_FULL + sb), (g >> 1) & 1)) { ok = false; break; }
+                if (!wait_warp(ctl, bar(ctl, B_S_FULL), g & 1)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t r0[32], r1[32];
-                tmem_ld32(tS + sb * 64, r0);
-                tmem_ld32(tS + sb * 64 + 32, r1);
+                tmem_ld32(tS, r0);
+                tmem_ld32(tS + 32, r1);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY + sb));
+                if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY));
 
-                // exchange partial scores with the peer CTA
-                if (g >= 1 && !wait_cluster_warp(ctl, bar(ctl, B_X_FREE), (g - 1) & 1)) { ok = false; break; }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_async_v4(peer_x + q * 16, __uint_as_float(r0[4 * q]),
-                                __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
-                                __uint_as_float(r0[4 * q + 3]), peer_x_full);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_async_v4(peer_x + 128 + q * 16, __uint_as_float(r1[4 * q]),
-                                __uint_as_float(r1[4 * q + 1]), __uint_as_float(r1[4 * q + 2]),
-                                __uint_as_float(r1[4 * q + 3]), peer_x_full);
-                mbar_arrive_expect_tx(bar(ctl, B_X_FULL), 256);
-                if (!wait_cluster_warp(ctl, bar(ctl, B_X_FULL), g & 1)) { ok = false; break; }
-                float s[64];
-                const float4 *xr = reinterpret_cast<const float4 *>(x_buf + h * kXRow);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 v = xr[q];
-                    s[4 * q] = v.x;
-                    s[4 * q + 1] = v.y;
-                    s[4 * q + 2] = v.z;
-                    s[4 * q + 3] = v.w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(peer_x_free);
-
-                // full scores (own + peer: the same sum on both CTAs), masked tail
                 const int valid = (k == n - 1) ? valid_last : kPage;
+                float s[64];
                 float m_loc = NEG_INF;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float a = (__uint_as_float(r0[j]) + s[j]) * P.scale_log2;
-                    float c = (__uint_as_float(r1[j]) + s[32 + j]) * P.scale_log2;
+                    float a = __uint_as_float(r0[j]) * P.scale_log2;
+                    float c = __uint_as_float(r1[j]) * P.scale_log2;
                     a = j < valid ? a : NEG_INF;
                     c = 32 + j < valid ? c : NEG_INF;
                     s[j] = a;
@@ -443,11 +437,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     m_run = m_loc;
                     need = true;
                 }
+                // probabilities -> bf16 (registers)
+                uint32_t pk[32];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float e0 = fast_exp2(s[2 * j] - m_run);
+                    const float e1 = fast_exp2(s[2 * j + 1] - m_run);
+                    lsum += e0 + e1;
+                    pk[j] = pack_bf16(e0, e1);
+                }
+                // PV(g-1) must be done before O is rescaled or P is overwritten
+                if (g >= 1 && !wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) { ok = false; break; }
                 if (__any_sync(0xffffffffu, need)) {
-                    if (!wait_warp(ctl, bar(ctl, B_PV_DONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
 #pragma unroll 1
                     for (int ch = 0; ch < 8; ++ch) {
@@ -460,47 +462,31 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         tmem_st32(tO + ch * 32, o);
                     }
                     tmem_wait_st();
-                    l_run *= alpha;
                 }
-                // probabilities -> bf16 -> TMEM
-                uint32_t pk[32];
-                float lsum = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float e0 = fast_exp2(s[2 * j] - m_run);
-                    const float e1 = fast_exp2(s[2 * j + 1] - m_run);
-                    lsum += e0 + e1;
-                    pk[j] = pack_bf16(e0, e1);
-                }
-                l_run += lsum;
-                if (g >= 2 && !wait_warp(ctl, bar(ctl, B_PV_DONE + sb), ((g - 2) >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
+                l_run = l_run * alpha + lsum;
                 tc_fence_after();
-                tmem_st32(tP + sb * 32, pk);
+                tmem_st32(tP, pk);
                 tmem_wait_st();
                 if (valid < kPage) {
-                    // zero the latent rows of the masked tail so that 0 * garbage stays 0
-                    uint8_t *stage = smem + kOffStage + (g % kStages) * kStageBytes;
-                    const int nchunk = (kPage - valid) * 4 * 8;  // 16-byte chunks
-                    for (int idx = (warp - 2) * 32 + lane; idx < nchunk; idx += 128) {
-                        const int blk = idx / ((kPage - valid) * 8);
-                        const int rem = idx % ((kPage - valid) * 8);
+                    // zero this CTA's latent rows of the masked tail so that 0 * garbage stays 0
+                    uint8_t *vbase = smem + kOffStage + (g % kStages) * kStageBytes + 4 * rank * kBlk;
+                    const int per_blk = (kPage - valid) * 8;  // 16-byte chunks per block
+                    for (int idx = (warp - 2) * 32 + lane; idx < 4 * per_blk; idx += 128) {
+                        const int blk = idx / per_blk, rem = idx % per_blk;
                         const int tok = valid + rem / 8;
-                        *reinterpret_cast<uint4 *>(stage + blk * kKvLatBlk + tok * 128 +
-                                                   (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vbase + blk * kBlk + tok * 128 + (rem % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_P_FULL + sb));
+                if (lane == 0) mbar_arrive(bar(ctl, B_P_FULL));
             }
             if (!ok) break;
 
             // epilogue: wait for the last PV, normalise, store this CTA's half
-            if (!wait_warp(ctl, bar(ctl, B_PV_DONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1)) break;
+            if (!wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) break;
             tc_fence_after();
             const float nan = __int_as_float(0x7fc00000);
             const float inv = bad ? nan : 1.f / l_run;
@@ -545,11 +531,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
-            (void)ii;
         }
     }
 
-    // teardown: both CTAs finish (no remote access in flight) before TMEM is freed
+    // teardown: both CTAs finish (no multicast or remote arrive in flight) before TMEM is freed
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -655,19 +640,18 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     {
         cuuint64_t dims[2] = {(cuuint64_t)kDr, qrows};
         cuuint64_t strides[1] = {(cuuint64_t)kDr * 2};
-        cuuint32_t box[2] = {32, 128};
-        if (!encode(&p.tm_q_rope, q_rope, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+        cuuint32_t box[2] = {64, 128};
+        if (!encode(&p.tm_q_rope, q_rope, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)kDrow, (cuuint64_t)kPage, (cuuint64_t)num_pages};
         cuuint64_t strides[2] = {(cuuint64_t)kDrow * 2, (cuuint64_t)kDrow * 2 * kPage};
-        cuuint32_t box_lat[3] = {64, 64, 1};
-        cuuint32_t box_rope[3] = {32, 64, 1};
-        if (!encode(&p.tm_kv_lat, kv, 3, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode(&p.tm_kv_rope, kv, 3, dims, strides, box_rope, CU_TENSOR_MAP_SWIZZLE_64B))
+        cuuint32_t box[3] = {64, 64, 1};
+        if (!encode(&p.tm_kv, kv, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
+    p.q_latent = static_cast<const __nv_bfloat16 *>(q_latent);
     p.block_table = block_table;
     p.ws = static_cast<uint8_t *>(ws);
     p.o_latent = static_cast<__nv_bfloat16 *>(o_latent);
