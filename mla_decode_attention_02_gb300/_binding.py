@@ -291,7 +291,7 @@ def plan_layout(batch: int, s_q: int, units: int) -> dict:
 _HDR = np.dtype([("magic", "<u4"), ("batch", "<i4"), ("s_q", "<i4"), ("max_pages", "<i4"),
                  ("num_units", "<i4"), ("num_rows", "<i4"), ("max_items", "<i4"),
                  ("num_items", "<i4"), ("num_parts", "<i4"), ("status", "<i4"),
-                 ("item_cost", "<i4"), ("min_split", "<i4"), ("total_cost", "<i8"),
+                 ("split", "<i4"), ("min_split", "<i4"), ("total_cost", "<i8"),
                  ("target", "<i8")])
 
 

@@ -18,6 +18,7 @@ cudaError_t launch_plan(const int32_t *seq_lens, void *ws, int32_t batch, int32_
 cudaError_t launch_combine(const void *ws, void *o_latent, float *lse, int32_t batch, int32_t s_q,
                            int32_t num_units, cudaStream_t stream);
 cudaError_t main_units(int32_t *units);
+bool plan_fits(int32_t rows, int32_t units);
 cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv,
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
@@ -93,6 +94,7 @@ mla_status mla_decode_plan(const mla_problem *prob, const int32_t *seq_lens, voi
     if (!seq_lens || !workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
     int32_t units = 0;
     if (mla::main_units(&units) != cudaSuccess) return MLA_ERR_CUDA;
+    if (!mla::plan_fits(prob->batch * prob->s_q, units)) return MLA_ERR_UNSUPPORTED;
     if (workspace_bytes < mla::plan_layout(prob->batch, prob->s_q, units).total)
         return MLA_ERR_WORKSPACE;
     cudaError_t e = mla::launch_plan(seq_lens, workspace, prob->batch, prob->s_q,

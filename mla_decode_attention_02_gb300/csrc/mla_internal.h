@@ -25,15 +25,17 @@ constexpr int kPage = MLA_PAGE_SIZE;     // tokens per cache page
 constexpr uint32_t kPlanMagic = 0x31414c4du;  // "MLA1"
 
 // Planner tuning, in units of one cache page of work: the fixed cost of a
-// work item (query load, pipeline fill, epilogue) and the shortest split.
+// work item (query load, pipeline fill, epilogue), the shortest split, and
+// the extra cost of splitting at all (fp32 partials written and merged).
 constexpr int kItemCost = 4;
 constexpr int kMinSplitPages = 8;
+constexpr int kSplitPenalty = 8;
 
 struct PlanHeader {  // 64 bytes at workspace offset 0
     uint32_t magic;
     int32_t batch, s_q, max_pages;
     int32_t num_units, num_rows, max_items, num_items;
-    int32_t num_parts, status, item_cost, min_split;
+    int32_t num_parts, status, split, min_split;  // split: rows may be cut (1) or not (0)
     int64_t total_cost, target;
 };
 static_assert(sizeof(PlanHeader) == 64, "header layout");
@@ -109,9 +111,15 @@ MLA_HD int64_t row_cost(int32_t pages) { return pages > 0 ? (int64_t)pages + kIt
 #pragma nv_exec_check_disable
 #endif
 template <typename Emit>
-MLA_HD int32_t cut_row(int64_t x0, int32_t pages, int64_t target, int32_t num_units, Emit emit) {
+MLA_HD int32_t cut_row(int64_t x0, int32_t pages, int64_t target, int32_t num_units, bool split,
+                       Emit emit) {
     if (pages <= 0) return 0;
     const int64_t cost = row_cost(pages);
+    if (!split) {  // whole row, on the unit whose stretch holds its midpoint
+        int64_t unit = (x0 + cost / 2) / target;
+        emit(0, 0, pages, (int32_t)(unit < num_units ? unit : num_units - 1));
+        return 1;
+    }
     int64_t unit = x0 / target;
     int64_t start = 0;
     int32_t n = 0;
@@ -128,6 +136,12 @@ MLA_HD int32_t cut_row(int64_t x0, int32_t pages, int64_t target, int32_t num_un
     }
     emit(n, (int32_t)start, pages, (int32_t)unit);
     return n + 1;
+}
+
+// Unit of a whole (unsplit) row: the one whose stretch holds its midpoint.
+MLA_HD int64_t mid_unit(int64_t x0, int64_t cost, int64_t target, int32_t num_units) {
+    int64_t u = (x0 + cost / 2) / target;
+    return u < num_units ? u : num_units - 1;
 }
 
 struct NoEmit {

@@ -19,14 +19,17 @@
 //   page g (64 tokens x 576) -> TMA multicast: CTA 0 loads dim blocks 0-4,
 //                               CTA 1 blocks 5-8, each into both CTAs
 //   S   = q . k^T            tcgen05 M=128 (heads) N=64 (tokens) K=576, fp32
-//                            in TMEM; q dims 0-319 are the A operand in TMEM,
-//                            dims 320-575 in shared memory
+//                            in TMEM, as two partial sums (dims 0-287 and
+//                            288-575) from two issuing warps; q dims 0-255
+//                            are the A operand in TMEM, 256-575 in shared memory
 //   P   = exp2(S*scale*log2e - m)    fp32 online softmax with a lazily
-//                            raised running max, rounded to bf16 into TMEM
-//   O_c += P . V_c           tcgen05 M=128 N=256 K=64, A = P from TMEM,
+//                            raised running max, rounded to bf16 into two
+//                            blocks of the page's stage that this CTA's PV
+//                            does not read
+//   O_c += P . V_c           tcgen05 M=128 N=256 K=64,
 //                            B = the page's latent dims [256c, 256c + 256)
 //
-// TMEM (512 columns): O half [0,256), S [256,320), P [320,352), q [352,512).
+// TMEM (512 columns): O half [0,256), S partials [256,384), q [384,512).
 // Warp roles per CTA: warp 0 issues TMA, warp 1 owns TMEM and issues the QK
 // MMAs, warp 6 issues the PV MMAs (one thread issues a tcgen05.mma about
 // every 27 ns, so the two chains get their own issuers), warps 2-5 (one
@@ -47,17 +50,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 224;       // warp 0 TMA, warp 1 QK MMA, warps 2-5 softmax, warp 6 PV MMA
-constexpr int kPvWarp = 6;
+constexpr int kThreads = 256;       // warp 0 TMA, warps 1/6 QK MMA, warps 2-5 softmax, warp 7 PV MMA
+constexpr int kQkbWarp = 6;
+constexpr int kPvWarp = 7;
 constexpr int kStages = 2;          // KV page ring (a full page per stage)
-constexpr int kPrefetch = 4;        // pages requested into L2 ahead of their stage load
+constexpr int kPrefetch = 2;        // L2 prefetch distance in pages (one beyond the stages)
 constexpr int kClusterSize = 2;
 constexpr uint16_t kBoth = 0x3;     // multicast mask: both CTAs of the pair
 constexpr uint32_t kBlk = 64 * 128;               // page block: 64 tokens x 64 dims (SW128)
 constexpr uint32_t kStageBytes = 9 * kBlk;        // dims 0-511 latent + 512-575 rope
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims (SW128)
-constexpr uint32_t kQSBytes = 4 * kQBlk;          // q dims 320-575 in shared memory
-constexpr int kQTDims = 320;                      // q dims 0-319 live in TMEM
+constexpr uint32_t kQSBytes = 5 * kQBlk;          // q dims 256-575 in shared memory
+constexpr int kQTDims = 256;                      // q dims 0-255 live in TMEM
 constexpr uint32_t kOffQS = 0;
 constexpr uint32_t kOffStage = kQSBytes;
 constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
@@ -67,9 +71,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
-constexpr uint32_t kColS = 256;     // 64 fp32 scores
-constexpr uint32_t kColP = 320;     // 32 columns of packed bf16 probabilities
-constexpr uint32_t kColQ = 352;     // 160 columns of packed bf16 q (dims 0-319)
+constexpr uint32_t kColS = 256;     // 2 x 64 fp32 partial scores (dims 0-287, 288-575)
+constexpr uint32_t kColQ = 384;     // 128 columns of packed bf16 q (dims 0-255)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
@@ -87,8 +90,9 @@ enum : uint32_t {
     B_P_FULL = B_S_EMPTY + 1,
     B_PV_DONE = B_P_FULL + 1,
     B_O_FREE = B_PV_DONE + 1,
-    B_DRAIN = B_O_FREE + 1,         // + issuer (0: QK, 1: PV)
-    B_COUNT = B_DRAIN + 2,
+    B_EPI = B_O_FREE + 1,           // 4 softmax warps done with the staged epilogue
+    B_DRAIN = B_EPI + 1,            // + issuer (0: QK a, 1: QK b, 2: PV)
+    B_COUNT = B_DRAIN + 3,
 };
 static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
 
@@ -182,18 +186,18 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(bar(ctl, B_Q_FULL), 5);
-        mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
+        mbar_init(bar(ctl, B_Q_EMPTY), 2 * kClusterSize);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(ctl, B_KV_FULL + s), 1);
             mbar_init(bar(ctl, B_KV_EMPTY + s), kClusterSize);
         }
-        mbar_init(bar(ctl, B_S_FULL), 1);
+        mbar_init(bar(ctl, B_S_FULL), 2);
         mbar_init(bar(ctl, B_S_EMPTY), 4);
         mbar_init(bar(ctl, B_P_FULL), 4);
         mbar_init(bar(ctl, B_PV_DONE), 1);
         mbar_init(bar(ctl, B_O_FREE), 4);
-        mbar_init(bar(ctl, B_DRAIN), 1);
-        mbar_init(bar(ctl, B_DRAIN + 1), 1);
+        mbar_init(bar(ctl, B_EPI), 4);
+        for (int d = 0; d < 3; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -236,27 +240,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            // q dims 320-575: both CTAs' copies must be free (last QK of the previous item)
-            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
-            if (lane == 0) {
-                const uint32_t fb = bar(ctl, B_Q_FULL);
-                mbar_arrive_expect_tx(fb, kQSBytes);
-                const int y = it.row * kHeads;
-                for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j) {
-                    if (j < 3)
-                        tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_lat, kQTDims + 64 * j, y, fb, kBoth);
-                    else
-                        tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
-                }
-            }
             bool ok = true;
-            const int kb0 = rank == 0 ? 0 : 5, kb1 = rank == 0 ? 5 : 9;  // this CTA's blocks
+            const int kb0 = rank == 0 ? 0 : 5, kb1 = rank == 0 ? 5 : 9;  // this CTA's page blocks
             const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
-            // pages [0, kPrefetch) of the item go to L2 at once
-            if (lane < min(kPrefetch, n)) {
-                const int pg = bt[lane];
-                for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, pg);
-            }
             for (int k0 = 0; k0 < n && ok; k0 += 32) {
                 const int mine = k0 + lane < n ? bt[k0 + lane] : 0;
                 const int ahead = k0 + lane + kPrefetch < n ? bt[k0 + lane + kPrefetch] : 0;
@@ -265,9 +251,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const int page = __shfl_sync(0xffffffffu, mine, kk);
                     const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
                     const uint32_t s = g % kStages;
-                    if (lane == 0 && k0 + kk + kPrefetch < n)
-                        for (int kb = kb0; kb < kb1; ++kb)
-                            tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, page_ahead);
                     // the stage is free in both CTAs (our loads write into both)
                     if (g >= kStages &&
                         !wait_warp(ctl, bar(ctl, B_KV_EMPTY + s), ((g / kStages) - 1) & 1)) {
@@ -283,52 +266,96 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         for (int kb = kb0; kb < kb1; ++kb)
                             tma_load_3d_mc(dst + kb * kBlk, &P.tm_kv, 64 * kb, 0, page, fb, kBoth);
                     }
+                    if (k0 + kk == 0) {
+                        // q dims 256-575, once the first page is on its way: both CTAs'
+                        // copies must be free (last QKs of the previous item done)
+                        if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            const uint32_t fb = bar(ctl, B_Q_FULL);
+                            mbar_arrive_expect_tx(fb, kQSBytes);
+                            const int y = it.row * kHeads;
+                            for (int j = rank == 0 ? 0 : 3; j < (rank == 0 ? 3 : 5); ++j) {
+                                if (j < 4)
+                                    tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_lat, kQTDims + 64 * j, y,
+                                                   fb, kBoth);
+                                else
+                                    tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                            }
+                        }
+                    }
+                    // warm L2 for a page beyond the two stages in flight
+                    if (lane == 0 && k0 + kk + kPrefetch < n)
+                        for (int kb = kb0; kb < kb1; ++kb)
+                            tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, page_ahead);
                     __syncwarp();
                 }
             }
             if (!ok) break;
         }
-    } else if (warp == 1 || warp == kPvWarp) {
+    } else if (warp == 1 || warp == kQkbWarp || warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuers
+        // One thread issues a tcgen05.mma about every 27 ns, so the score
+        // contraction is split over two issuers with separate accumulators
+        // (dims 0-287 and 288-575, summed by the softmax in a fixed order)
+        // and the PV product gets a third.
         if (lane == 0) {
-            const bool qk_role = warp == 1;
+            const int role = warp == 1 ? 0 : (warp == kQkbWarp ? 1 : 2);
             // Descriptor bases; every MMA below adds a compile-time byte offset (>> 4).
             const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
             const uint64_t d_kv0 = smem_desc(s_stage, 16, 1024, 2);
             const uint64_t d_v0 = smem_desc(s_stage + 4 * rank * kBlk, 8192, 1024, 2);
+            const uint64_t d_p0 = smem_desc(s_stage + (rank == 0 ? 7 : 0) * kBlk, 16, 1024, 2);
             constexpr uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
-            const uint32_t tS = tmem + kColS, tQ = tmem + kColQ, tO = tmem + kColO, tP = tmem + kColP;
+            const uint32_t tSa = tmem + kColS, tSb = tmem + kColS + 64, tQ = tmem + kColQ;
+            const uint32_t tO = tmem + kColO;
             uint32_t g = 0;
             bool ok = true;
             for (int i = i_begin; i < i_end && ok; ++i) {
                 const WorkItem it = items[i];
                 const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
                 const uint32_t ii = (uint32_t)(i - i_begin);
-                if (qk_role && !wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+                if (role < 2 && !wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
                 for (int k = 0; k < n && ok; ++k, ++g) {
                     const uint32_t s = g % kStages;
                     const uint64_t stage_off = (uint64_t)((s * kStageBytes) >> 4);
-                    if (qk_role) {
-                        // S = q . k^T over all 576 dims
+                    if (role < 2) {
                         if (!wait(ctl, bar(ctl, B_KV_FULL + s), (g / kStages) & 1)) { ok = false; break; }
                         if (g >= 1 && !wait(ctl, bar(ctl, B_S_EMPTY), (g - 1) & 1)) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t kv = d_kv0 + stage_off;
+                        if (role == 0) {
+                            // S_a: dims 0-255 (q from TMEM) and 256-287 (q block 0, k-steps 0-1)
 #pragma unroll
-                        for (int ks = 0; ks < kQTDims / 16; ++ks)  // q from TMEM, dims 0-319
-                            mma_ts(tS, tQ + 8 * ks,
-                                   kv + (uint64_t)(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4), id_qk,
-                                   ks > 0 ? 1u : 0u);
+                            for (int ks = 0; ks < 16; ++ks)
+                                mma_ts(tSa, tQ + 8 * ks,
+                                       kv + (uint64_t)(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4),
+                                       id_qk, ks > 0 ? 1u : 0u);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)               // q from smem, dims 320-575
-                            mma_ss(tS, d_qs + (uint64_t)(((j >> 2) * kQBlk + (j & 3) * 32) >> 4),
-                                   kv + (uint64_t)(((5 + (j >> 2)) * kBlk + (j & 3) * 32) >> 4),
-                                   id_qk, 1u);
+                            for (int ks = 0; ks < 2; ++ks)
+                                mma_ss(tSa, d_qs + (uint64_t)((ks * 32) >> 4),
+                                       kv + (uint64_t)((4 * kBlk + ks * 32) >> 4), id_qk, 1u);
+                        } else {
+                            // S_b: dims 288-319 (q block 0, k-steps 2-3) and 320-575 (q blocks 1-4)
+#pragma unroll
+                            for (int ks = 2; ks < 4; ++ks)
+                                mma_ss(tSb, d_qs + (uint64_t)((ks * 32) >> 4),
+                                       kv + (uint64_t)((4 * kBlk + ks * 32) >> 4), id_qk,
+                                       ks > 2 ? 1u : 0u);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                mma_ss(tSb,
+                                       d_qs + (uint64_t)(((1 + (j >> 2)) * kQBlk + (j & 3) * 32) >> 4),
+                                       kv + (uint64_t)(((5 + (j >> 2)) * kBlk + (j & 3) * 32) >> 4),
+                                       id_qk, 1u);
+                        }
                         mma_commit(bar(ctl, B_S_FULL));
                         if (k == n - 1) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
                     } else {
-                        // O_c (+)= P . V_c
+                        // O_c (+)= P . V_c, P (bf16) in two spare blocks of the page's stage
                         if (!wait(ctl, bar(ctl, B_P_FULL), g & 1)) { ok = false; break; }
                         if (k == 0 && ii > 0 && !wait(ctl, bar(ctl, B_O_FREE), (ii - 1) & 1)) {
                             ok = false;
@@ -336,17 +363,20 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         }
                         tc_fence_after();
                         const uint64_t v = d_v0 + stage_off;
+                        const uint64_t pa = d_p0 + stage_off;
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(tO, tP + ks * 8, v + (uint64_t)((ks * 2048) >> 4), id_pv,
-                                   (k == 0 && ks == 0) ? 0u : 1u);
+                            mma_ss(tO, pa + (uint64_t)((ks * 32) >> 4), v + (uint64_t)((ks * 2048) >> 4),
+                                   id_pv, (k == 0 && ks == 0) ? 0u : 1u);
                         mma_commit(bar(ctl, B_PV_DONE));
-                        mma_commit_mc(bar(ctl, B_KV_EMPTY + s), kBoth);
+                        // the last page's stage is released by the epilogue, which stages
+                        // the output through it
+                        if (k != n - 1) mma_commit_mc(bar(ctl, B_KV_EMPTY + s), kBoth);
                     }
                 }
             }
             // wind down: every MMA this thread issued completes before TMEM is freed
-            const uint32_t drain = bar(ctl, B_DRAIN + (qk_role ? 0 : 1));
+            const uint32_t drain = bar(ctl, B_DRAIN + role);
             mma_commit(drain);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
@@ -359,7 +389,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const int h = quarter * 32 + lane;         // head = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + kColS;
-        const uint32_t tP = tmem + lane_off + kColP;
         const uint32_t tO = tmem + lane_off + kColO;
         const uint32_t tQ = tmem + lane_off + kColQ;
         const float NEG_INF = -INFINITY;
@@ -373,13 +402,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q dims 0-319 of this head -> TMEM (the A operand of the first 20 k-steps)
+            // q dims 0-255 of this head -> TMEM (the A operand of the first 16 k-steps)
             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
             {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     P.q_latent + ((size_t)it.row * kHeads + h) * kDl);
 #pragma unroll 1
-                for (int c = 0; c < 5; ++c) {
+                for (int c = 0; c < kQTDims / 64; ++c) {
                     uint32_t q[32];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
@@ -410,6 +439,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 tmem_ld32(tS, r0);
                 tmem_ld32(tS + 32, r1);
                 tmem_wait_ld();
+                {   // add the second partial (dims 288-575): the same order in both CTAs
+                    uint32_t t[32];
+                    tmem_ld32(tS + 64, t);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r0[j] = __float_as_uint(__uint_as_float(r0[j]) + __uint_as_float(t[j]));
+                    tmem_ld32(tS + 96, t);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r1[j] = __float_as_uint(__uint_as_float(r1[j]) + __uint_as_float(t[j]));
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY));
@@ -464,9 +506,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     tmem_wait_st();
                 }
                 l_run = l_run * alpha + lsum;
-                tc_fence_after();
-                tmem_st32(tP, pk);
-                tmem_wait_st();
+                {   // P row -> the stage's spare blocks, K-major with the 128-byte swizzle
+                    uint8_t *prow = smem + kOffStage + (g % kStages) * kStageBytes +
+                                    (rank == 0 ? 7 : 0) * kBlk + h * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
                 if (valid < kPage) {
                     // zero this CTA's latent rows of the masked tail so that 0 * garbage stays 0
                     uint8_t *vbase = smem + kOffStage + (g % kStages) * kStageBytes + 4 * rank * kBlk;
@@ -477,60 +524,97 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         *reinterpret_cast<uint4 *>(vbase + blk * kBlk + tok * 128 + (rem % 8) * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
-                    fence_proxy_async_smem();
                 }
+                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_P_FULL));
             }
             if (!ok) break;
 
-            // epilogue: wait for the last PV, normalise, store this CTA's half
+            // epilogue: wait for the last PV, normalise, store this CTA's half.  The
+            // rows go through the last page's stage (free now: its QK and PV are done
+            // and it is only refilled after this epilogue releases it) so that every
+            // global store writes 512 contiguous bytes of one row.
             if (!wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) break;
             tc_fence_after();
             const float nan = __int_as_float(0x7fc00000);
             const float inv = bad ? nan : 1.f / l_run;
             const float lse = bad ? nan : (m_run + log2f(l_run)) * 0.69314718055994531f;
-            const size_t hrow = (size_t)it.row * kHeads + h;
-            if (it.part < 0) {
-                uint4 *dst = reinterpret_cast<uint4 *>(P.o_latent + hrow * kDl + rank * 256);
+            const uint32_t s_last = (g - 1) % kStages;
+            uint8_t *stg = smem + kOffStage + s_last * kStageBytes + quarter * 16384;  // 32 rows x 512 B
+            uint8_t *my_stg = stg + lane * 512;
+            const bool final_out = it.part < 0;
+            const int passes = final_out ? 1 : 2;   // 512 B of a row per pass
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + ch * 32, o);
-                    tmem_wait_ld();
+            for (int pass = 0; pass < passes; ++pass) {
+                // TMEM -> normalised values -> swizzled staging row (chunk c at c ^ lane)
+                if (final_out) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + ch * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                        dst[ch * 4 + q] = v;
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                            v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                            v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                            v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                            const int c = ch * 4 + q;
+                            *reinterpret_cast<uint4 *>(my_stg + ((c ^ lane) << 4)) = v;
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + (pass * 4 + ch) * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int c = ch * 8 + q;
+                            *reinterpret_cast<float4 *>(my_stg + ((c ^ lane) << 4)) =
+                                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+                        }
                     }
                 }
-                if (rank == 0) P.lse[hrow] = lse;
-            } else {
-                const size_t slot = (size_t)it.part * kHeads + h;
-                float4 *dst = reinterpret_cast<float4 *>(o_part + slot * kDl + rank * 256);
-#pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + ch * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[ch * 8 + q] = make_float4(__uint_as_float(o[4 * q]) * inv,
-                                                      __uint_as_float(o[4 * q + 1]) * inv,
-                                                      __uint_as_float(o[4 * q + 2]) * inv,
-                                                      __uint_as_float(o[4 * q + 3]) * inv);
+                if (pass == passes - 1) {  // O fully read: the next item's PV may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
                 }
-                if (rank == 0) lse_part[slot] = lse;
+                __syncwarp();
+                // staging -> global, one row per step, 32 lanes x 16 B contiguous
+#pragma unroll 4
+                for (int r = 0; r < 32; ++r) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 512 + ((lane ^ r) << 4));
+                    const size_t hr = (size_t)it.row * kHeads + quarter * 32 + r;
+                    if (final_out) {
+                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256)[lane] = v;
+                    } else {
+                        const size_t slot = (size_t)it.part * kHeads + quarter * 32 + r;
+                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + pass * 128)[lane] = v;
+                    }
+                }
+                __syncwarp();
+            }
+            if (rank == 0) {
+                if (final_out) P.lse[(size_t)it.row * kHeads + h] = lse;
+                else lse_part[(size_t)it.part * kHeads + h] = lse;
             }
             if (bad && lane == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
-            tc_fence_before();
+            // once all four softmax warps are done with the stage, release it in both CTAs
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
+            if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
+            if (warp == 2 && !wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
+            if (warp == 2 && lane == 0) {
+                mbar_arrive(bar(ctl, B_KV_EMPTY + s_last));
+                mbar_arrive_cluster(mapa(bar(ctl, B_KV_EMPTY + s_last), rank ^ 1u));
+            }
         }
     }
 

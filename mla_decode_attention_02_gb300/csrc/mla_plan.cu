@@ -11,8 +11,11 @@
 //
 // Every row (request b, query token t) costs pages + kItemCost on a cost
 // line laid out in row order; the line is cut into num_units stretches of
-// `target` = ceil(total / num_units), and each row is cut where a stretch
-// boundary falls inside it (cut_row).  Rows keep their order, items are
+// `target` = ceil(total / num_units).  If no row is much longer than a
+// stretch, rows stay whole and each goes to the unit whose stretch holds its
+// midpoint (no partial outputs, no merge); otherwise each row is cut where a
+// stretch boundary falls inside it (cut_row).  The choice compares the
+// largest unit load without cuts against target + kItemCost + kSplitPenalty.  Rows keep their order, items are
 // emitted in row order, and units come out non-decreasing, so the unit of
 // every item follows from prefix sums alone: no atomics, no sorting, and
 // the same bytes on every run.  The host twin below runs the identical
@@ -20,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "mla_internal.h"
 
@@ -27,6 +31,8 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr size_t kMaxPlanSmem = 200 * 1024;  // per-row working set of the planner kernel
+
 
 // Inclusive block-wide sum of one int64 per thread (1024 threads).
 __device__ int64_t block_inclusive_sum(int64_t v, int64_t *warp_sums) {
@@ -53,13 +59,24 @@ __device__ int64_t block_inclusive_sum(int64_t v, int64_t *warp_sums) {
     return r;
 }
 
+// Shared-memory bytes the planner kernel needs for R rows and U units.
+size_t plan_smem_bytes(int32_t R, int32_t U) {
+    return sizeof(int64_t) * ((size_t)R + U) + sizeof(int32_t) * (2 * (size_t)R + U);
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1)
 mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, int32_t batch,
                 int32_t s_q, int32_t max_pages, int32_t num_units) {
     __shared__ int64_t warp_sums[32];
-    __shared__ int64_t carry, carry_parts;
+    __shared__ int64_t carry, carry_parts, max_load;
     __shared__ int32_t bad;
+    extern __shared__ int64_t plan_smem[];
     const PlanLayout L = plan_layout(batch, s_q, num_units);
+    const int32_t R = L.num_rows;
+    int64_t *s_pos = plan_smem;                                        // [R] cost-line start
+    int64_t *first_pos = s_pos + R;                                    // [U] (no-split runs)
+    int32_t *s_pages = reinterpret_cast<int32_t *>(first_pos + num_units);  // [R]
+    int32_t *s_unit = s_pages + R;                                     // [R + U] unit of each item
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws);
     WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
     int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
@@ -68,12 +85,12 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     int32_t *row_part0 = reinterpret_cast<int32_t *>(ws + L.row_part0);
     int32_t *row_item0 = reinterpret_cast<int32_t *>(ws + L.row_item0);
     int64_t *row_pos = reinterpret_cast<int64_t *>(ws + L.row_pos);
-    const int32_t R = L.num_rows;
 
-    // Pass 1: cost-line position of every row (exclusive prefix of row costs).
+    // Pass 1: pages of every row and its cost-line position (exclusive prefix of costs).
     if (threadIdx.x == 0) {
         carry = 0;
         carry_parts = 0;
+        max_load = 0;
         bad = 0;
     }
     __syncthreads();
@@ -83,10 +100,14 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
         if (r < R) {
             const int32_t p = row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages);
             if (p < 0) bad = 1;
+            s_pages[r] = p;
             c = row_cost(p);
         }
         const int64_t incl = block_inclusive_sum(c, warp_sums);
-        if (r < R) row_pos[r] = carry + incl - c;
+        if (r < R) {
+            s_pos[r] = carry + incl - c;
+            row_pos[r] = carry + incl - c;
+        }
         __syncthreads();
         if (threadIdx.x == kPlanThreads - 1) carry += incl;
         __syncthreads();
@@ -94,24 +115,61 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     const int64_t total = carry;
     const int64_t target = total > 0 ? (total + num_units - 1) / num_units : 1;
     __syncthreads();
+
+    // Pass 1b: largest unit load if no row is cut (rows on their midpoint units).
+    for (int32_t r = threadIdx.x; r < R; r += kPlanThreads) {
+        const int64_t u = mid_unit(s_pos[r], row_cost(s_pages[r]), target, num_units);
+        if (r == 0 || mid_unit(s_pos[r - 1], row_cost(s_pages[r - 1]), target, num_units) != u)
+            first_pos[u] = s_pos[r];
+    }
+    __syncthreads();
+    {
+        int64_t my_max = 0;
+        for (int32_t r = threadIdx.x; r < R; r += kPlanThreads) {
+            const int64_t c = row_cost(s_pages[r]);
+            const int64_t u = mid_unit(s_pos[r], c, target, num_units);
+            if (r == R - 1 ||
+                mid_unit(s_pos[r + 1], row_cost(s_pages[r + 1]), target, num_units) != u) {
+                const int64_t load = s_pos[r] + c - first_pos[u];
+                my_max = load > my_max ? load : my_max;
+            }
+        }
+        atomicMax(reinterpret_cast<unsigned long long *>(&max_load), (unsigned long long)my_max);
+    }
+    __syncthreads();
+    const bool split = target + kItemCost + kSplitPenalty < max_load;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
 
-    // Pass 2: pieces per row -> first item and first partial slot of each row.
+    // Pass 2: pieces per row -> first item and first partial slot; emit the items.
     for (int32_t base = 0; base < R; base += kPlanThreads) {
         const int32_t r = base + threadIdx.x;
         int64_t n = 0, np = 0;
         if (r < R) {
-            const int32_t p = row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages);
-            n = cut_row(row_pos[r], p, target, num_units, NoEmit{});
+            n = cut_row(s_pos[r], s_pages[r], target, num_units, split, NoEmit{});
             np = n > 1 ? n : 0;
         }
         const int64_t incl_n = block_inclusive_sum(n, warp_sums);
         const int64_t incl_p = block_inclusive_sum(np, warp_sums);
         if (r < R) {
-            row_item0[r] = (int32_t)(carry + incl_n - n);
-            row_part0[r] = n > 1 ? (int32_t)(carry_parts + incl_p - np) : -1;
+            const int32_t first = (int32_t)(carry + incl_n - n);
+            const int32_t part0 = n > 1 ? (int32_t)(carry_parts + incl_p - np) : -1;
+            row_item0[r] = first;
+            row_part0[r] = part0;
             row_nparts[r] = (int32_t)n;
+            const int32_t t = r % s_q;
+            const int32_t vis = s_pages[r] > 0 ? seq_lens[r / s_q] - s_q + 1 + t : 0;
+            cut_row(s_pos[r], s_pages[r], target, num_units, split,
+                    [&](int32_t i, int32_t pg0, int32_t pg1, int32_t unit) {
+                        WorkItem it;
+                        it.row = r;
+                        it.kv_begin = pg0 * kPage;
+                        it.kv_end = min(pg1 * kPage, vis);
+                        it.part = part0 >= 0 ? part0 + i : -1;
+                        items[first + i] = it;
+                        item_unit[first + i] = unit;
+                        s_unit[first + i] = unit;
+                    });
         }
         __syncthreads();
         if (threadIdx.x == kPlanThreads - 1) {
@@ -123,31 +181,11 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     const int32_t num_items = (int32_t)carry;
     const int32_t num_parts = (int32_t)carry_parts;
 
-    // Pass 3: emit every row's items and the unit each one runs on.
-    for (int32_t r = threadIdx.x; r < R; r += kPlanThreads) {
-        const int32_t b = r / s_q, t = r % s_q;
-        const int32_t p = row_pages(seq_lens[b], s_q, t, max_pages);
-        const int32_t first = row_item0[r];
-        const int32_t part0 = row_part0[r];
-        const int32_t vis = p > 0 ? seq_lens[b] - s_q + 1 + t : 0;
-        cut_row(row_pos[r], p, target, num_units,
-                [&](int32_t i, int32_t pg0, int32_t pg1, int32_t unit) {
-                    WorkItem it;
-                    it.row = r;
-                    it.kv_begin = pg0 * kPage;
-                    it.kv_end = min(pg1 * kPage, vis);
-                    it.part = part0 >= 0 ? part0 + i : -1;
-                    items[first + i] = it;
-                    item_unit[first + i] = unit;
-                });
-    }
-    __syncthreads();
-
-    // Pass 4: unit_begin[u] = first item whose unit is >= u (units are
+    // Pass 3: unit_begin[u] = first item whose unit is >= u (units are
     // non-decreasing along the items).
     for (int32_t i = threadIdx.x; i < num_items; i += kPlanThreads) {
-        const int32_t u = item_unit[i];
-        const int32_t u_prev = i > 0 ? item_unit[i - 1] : -1;
+        const int32_t u = s_unit[i];
+        const int32_t u_prev = i > 0 ? s_unit[i - 1] : -1;
         for (int32_t v = u_prev + 1; v <= u; ++v) unit_begin[v] = i;
         if (i == num_items - 1)
             for (int32_t v = u + 1; v <= num_units; ++v) unit_begin[v] = num_items;
@@ -167,7 +205,7 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
         h.num_items = num_items;
         h.num_parts = num_parts;
         h.status = bad ? MLA_DEV_BAD_SEQ_LEN : 0;
-        h.item_cost = kItemCost;
+        h.split = split ? 1 : 0;
         h.min_split = kMinSplitPages;
         h.total_cost = total;
         h.target = target;
@@ -200,14 +238,27 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
         total += row_cost(p);
     }
     const int64_t target = total > 0 ? (total + num_units - 1) / num_units : 1;
+    // largest unit load if no row is cut (rows on their midpoint units)
+    int64_t max_load = 0, run_first = 0, run_unit = -1;
+    for (int32_t r = 0; r < R; ++r) {
+        const int64_t c = row_cost(row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages));
+        const int64_t u = mid_unit(row_pos[r], c, target, num_units);
+        if (u != run_unit) {
+            run_unit = u;
+            run_first = row_pos[r];
+        }
+        const int64_t load = row_pos[r] + c - run_first;
+        if (load > max_load) max_load = load;
+    }
+    const bool split = target + kItemCost + kSplitPenalty < max_load;
     int32_t n_items = 0, n_parts = 0, last_unit = -1;
     for (int32_t r = 0; r < R; ++r) {
         const int32_t b = r / s_q, t = r % s_q;
         const int32_t p = row_pages(seq_lens[b], s_q, t, max_pages);
-        const int32_t n = cut_row(row_pos[r], p, target, num_units, NoEmit{});
+        const int32_t n = cut_row(row_pos[r], p, target, num_units, split, NoEmit{});
         const int32_t part0 = n > 1 ? n_parts : -1;
         const int32_t vis = p > 0 ? seq_lens[b] - s_q + 1 + t : 0;
-        cut_row(row_pos[r], p, target, num_units,
+        cut_row(row_pos[r], p, target, num_units, split,
                 [&](int32_t i, int32_t pg0, int32_t pg1, int32_t unit) {
                     WorkItem it;
                     it.row = r;
@@ -237,7 +288,7 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
     h.num_items = n_items;
     h.num_parts = n_parts;
     h.status = bad ? MLA_DEV_BAD_SEQ_LEN : 0;
-    h.item_cost = kItemCost;
+    h.split = split ? 1 : 0;
     h.min_split = kMinSplitPages;
     h.total_cost = total;
     h.target = target;
@@ -247,9 +298,20 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
 
 cudaError_t launch_plan(const int32_t *seq_lens, void *ws, int32_t batch, int32_t s_q,
                         int32_t max_pages, int32_t num_units, cudaStream_t stream) {
-    mla_plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, static_cast<uint8_t *>(ws), batch,
-                                                    s_q, max_pages, num_units);
+    const size_t smem = plan_smem_bytes(batch * s_q, num_units);
+    if (smem > kMaxPlanSmem) return cudaErrorInvalidValue;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(mla_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kMaxPlanSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    mla_plan_kernel<<<1, kPlanThreads, smem, stream>>>(seq_lens, static_cast<uint8_t *>(ws), batch,
+                                                       s_q, max_pages, num_units);
     return cudaGetLastError();
 }
+
+bool plan_fits(int32_t rows, int32_t units) { return plan_smem_bytes(rows, units) <= kMaxPlanSmem; }
 
 }  // namespace mla
