@@ -52,6 +52,8 @@ def _args():
     ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps eagerly instead of from one captured CUDA graph")
     return ap.parse_args()
 
 
@@ -65,12 +67,7 @@ def _dist():
 _CUDART = None
 
 
-def _event_ms(e0, e1) -> float:
-    """cudaEventElapsedTime on torch events that the library recorded through the C ABI.
-
-    torch only reports elapsed time for events it recorded itself, so this asks the
-    CUDA runtime that torch already loaded.
-    """
+def _cudart():
     import ctypes
     global _CUDART
     if _CUDART is None:
@@ -88,9 +85,31 @@ def _event_ms(e0, e1) -> float:
             _CUDART = ctypes.CDLL(cands[0])
         _CUDART.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
                                                  ctypes.c_void_p]
+        _CUDART.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_uint]
+    return _CUDART
+
+
+def _record(ev, stream, external: bool) -> None:
+    """Record a torch event on `stream`; as an external node when capturing a graph."""
+    import ctypes
+    rc = _cudart().cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event),
+                                             ctypes.c_void_p(stream.cuda_stream),
+                                             1 if external else 0)
+    if rc != 0:
+        raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
+
+
+def _event_ms(e0, e1) -> float:
+    """cudaEventElapsedTime on torch events that the library recorded through the C ABI.
+
+    torch only reports elapsed time for events it recorded itself, so this asks the
+    CUDA runtime that torch already loaded.
+    """
+    import ctypes
     ms = ctypes.c_float(0.0)
-    rc = _CUDART.cudaEventElapsedTime(ctypes.byref(ms), ctypes.c_void_p(e0.cuda_event),
-                                      ctypes.c_void_p(e1.cuda_event))
+    rc = _cudart().cudaEventElapsedTime(ctypes.byref(ms), ctypes.c_void_p(e0.cuda_event),
+                                        ctypes.c_void_p(e1.cuda_event))
     if rc != 0:
         raise RuntimeError(f"cudaEventElapsedTime failed ({rc})")
     return ms.value
@@ -306,15 +325,16 @@ def run_native(args, rank, world, local):
 
     steps = args.steps
     if steps is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(5):
-            flush.fill_(1)
-            step()
-        e1.record()
-        torch.cuda.synchronize()
-        per = e0.elapsed_time(e1) / 5 / 1e3
-        steps = int(min(20000, max(20, 3.0 / max(per, 1e-6))))
+        for _ in range(2):  # the first pass still pays one-time costs; keep the second
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                flush.fill_(1)
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            per = e0.elapsed_time(e1) / 5 / 1e3
+        steps = int(min(4000 if not args.no_graph else 20000, max(20, 3.0 / max(per, 1e-6))))
         if world > 1:
             t = torch.tensor([steps], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MIN)
@@ -324,9 +344,10 @@ def run_native(args, rank, world, local):
     ev_s = [mk() for _ in range(steps)]
     ev_e = [mk() for _ in range(steps)]
     ev_k = [[mk(), mk(), mk()] for _ in range(steps)]
-    for evs in ev_k:          # torch creates the CUDA event on first record; the library
-        for e in evs:         # re-records these through the C ABI inside the timed loop
-            e.record(stream)
+    # torch creates each CUDA event on its first record; the timed loop re-records them
+    # through the CUDA runtime (and the library, through the C ABI)
+    for e in ev_s + ev_e + [x for evs in ev_k for x in evs]:
+        e.record(stream)
     torch.cuda.synchronize()
 
     gpu_id = None
@@ -334,24 +355,51 @@ def run_native(args, rank, world, local):
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
+
+    def timed_steps(external: bool, phases: bool):
+        cur = torch.cuda.current_stream()
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            _record(ev_s[k], cur, external)
+            step(events=ev_k[k] if phases else None)
+            _record(ev_e[k], cur, external)
+
+    # Two timed regions over the same K steps.  (1) step boundaries only: the
+    # step time (planner, main kernel and merge overlap their launches by
+    # programmatic dependent launch, which events between the kernels would
+    # serialise).  (2) with events around each kernel: the per-kernel times
+    # behind the roofline figure.
+    graphs = []
+    if not args.no_graph:
+        for phases in (False, True):
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                timed_steps(external=True, phases=phases)
+            graphs.append(g_)
+        torch.cuda.synchronize()
+
+    def run_region(phases: bool):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if graphs:
+            graphs[1 if phases else 0].replay()
+        else:
+            timed_steps(external=False, phases=phases)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     time.sleep(0.5)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     t_start = time.time()
-    for k in range(steps):
-        flush.fill_(k & 0xFF)
-        ev_s[k].record(stream)
-        step(events=ev_k[k])
-        ev_e[k].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    run_region(phases=False)
     t_end = time.time()
     clocks = sampler.summary(t_start, t_end) if sampler else None
-
     step_ms = statistics.mean(_event_ms(ev_s[k], ev_e[k]) for k in range(steps))
+    run_region(phases=True)
+    phase_step_ms = statistics.mean(_event_ms(ev_s[k], ev_e[k]) for k in range(steps))
+
     main_ms = statistics.mean(_event_ms(ev_k[k][0], ev_k[k][1]) for k in range(steps))
     comb_ms = statistics.mean(_event_ms(ev_k[k][1], ev_k[k][2]) for k in range(steps))
     plan_ms = statistics.mean(_event_ms(ev_s[k], ev_k[k][0]) for k in range(steps))
@@ -442,12 +490,14 @@ def run_native(args, rank, world, local):
                 "tflops": world * fl / (step_ms * 1e-3) / 1e12,
                 "us_per_step": step_ms * 1e3,
                 "phases_us": {"plan": plan_ms * 1e3, "main": main_ms * 1e3,
-                              "combine": comb_ms * 1e3},
+                              "combine": comb_ms * 1e3,
+                              "step_with_phase_events": phase_step_ms * 1e3},
                 "roofline_frac_8tbs": t_roof / (step_ms * 1e-3),
                 "roofline_frac_measured_peaks": t_roof_meas / (step_ms * 1e-3),
                 "e2e": e2e, "gpu_launches": 3 * steps, "roofline": roof,
                 "cpu_baseline": cpu_base, "clocks": clocks,
-                "device": torch.cuda.get_device_name(dev), "units": mla.num_units()}
+                "device": torch.cuda.get_device_name(dev), "units": mla.num_units(),
+                "launch": "eager" if args.no_graph else "cuda_graph"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

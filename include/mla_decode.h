@@ -142,7 +142,9 @@ mla_status mla_decode(const mla_problem *prob, const void *q_latent, const void 
  * mla_decode with phase timing for profiling tools: records events[0] on
  * `stream` before the main kernel, events[1] after it (before the merge)
  * and events[2] after the merge.  events points to 3 cudaEvent_t handles
- * created by the caller; NULL entries are skipped.  Same contract as
+ * created by the caller; NULL entries are skipped.  Under stream capture the
+ * records are external event nodes (cudaEventRecordExternal), so the
+ * timestamps can be read after the graph is launched.  Same contract as
  * mla_decode otherwise.
  */
 mla_status mla_decode_timed(const mla_problem *prob, const void *q_latent, const void *q_rope,

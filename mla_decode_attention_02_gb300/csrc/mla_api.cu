@@ -119,9 +119,16 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
     if (workspace_bytes < mla::plan_layout(prob->batch, prob->s_q, units).total)
         return MLA_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Inside stream capture the events become external record nodes, so their
+    // timestamps stay readable after the graph runs.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (events && cudaStreamIsCapturing(s, &capture) != cudaSuccess) return MLA_ERR_CUDA;
     auto mark = [&](int i) -> bool {
         if (!events || !events[i]) return true;
-        return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+        cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+        if (capture == cudaStreamCaptureStatusActive)
+            return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) == cudaSuccess;
+        return cudaEventRecord(ev, s) == cudaSuccess;
     };
     if (!mark(0)) return MLA_ERR_CUDA;
     cudaError_t e = mla::launch_main(q_latent, q_rope, kv_cache, num_pages, block_table, scale,

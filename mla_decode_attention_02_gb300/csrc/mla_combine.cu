@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "mla_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -25,6 +26,8 @@ constexpr int kCombineGrid = 1024;  // CTAs; warps stride over (row, head) tasks
 __global__ void __launch_bounds__(32 * kCombineWarps)
 mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o_latent,
                    float *__restrict__ lse_out, int32_t batch, int32_t s_q, int32_t num_units) {
+    // launched as a programmatic dependent of the main kernel
+    ptx::pdl_wait_prior();
     const PlanLayout L = plan_layout(batch, s_q, num_units);
     const int32_t lane = threadIdx.x & 31;
     const int64_t tasks = (int64_t)L.num_rows * kHeads;
@@ -92,10 +95,17 @@ cudaError_t launch_combine(const void *ws, void *o_latent, float *lse, int32_t b
     const int64_t tasks = (int64_t)batch * s_q * kHeads;
     const int64_t need = (tasks + kCombineWarps - 1) / kCombineWarps;
     const int grid = (int)(need < kCombineGrid ? need : kCombineGrid);
-    mla_combine_kernel<<<grid, 32 * kCombineWarps, 0, stream>>>(
-        static_cast<const uint8_t *>(ws), static_cast<__nv_bfloat16 *>(o_latent), lse, batch, s_q,
-        num_units);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * kCombineWarps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_combine_kernel, static_cast<const uint8_t *>(ws),
+                              static_cast<__nv_bfloat16 *>(o_latent), lse, batch, s_q, num_units);
 }
 
 }  // namespace mla

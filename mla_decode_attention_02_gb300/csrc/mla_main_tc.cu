@@ -30,10 +30,12 @@
 //                            B = the page's latent dims [256c, 256c + 256)
 //
 // TMEM (512 columns): O half [0,256), S partials [256,384), q [384,512).
-// Warp roles per CTA: warp 0 issues TMA, warp 1 owns TMEM and issues the QK
-// MMAs, warp 6 issues the PV MMAs (one thread issues a tcgen05.mma about
-// every 27 ns, so the two chains get their own issuers), warps 2-5 (one
-// thread per head) load q into TMEM and run the softmax and the epilogue.  Every wait is bounded: on time-out the kernel
+// Warp roles per CTA: warp 0 issues TMA; warps 1 and 6 issue the two QK
+// partial sums and warp 7 the PV product (one thread issues a tcgen05.mma
+// about every 27 ns, so each chain gets its own issuer); warp 1 also owns
+// TMEM; warps 2-5 and 8-11 (two per TMEM lane quarter, one thread per head
+// and half of the columns) load q into TMEM and run the softmax and the
+// epilogue.  Every wait is bounded: on time-out the kernel
 // records MLA_DEV_TIMEOUT and winds down instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,7 +52,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;       // warp 0 TMA, warps 1/6 QK MMA, warps 2-5 softmax, warp 7 PV MMA
+constexpr int kThreads = 384;       // warp 0 TMA, warps 1/6 QK MMA, 7 PV MMA, 2-5 + 8-11 softmax
+constexpr int kSoftmaxWarps = 8;    // two per TMEM lane quarter, 32 score columns each
 constexpr int kQkbWarp = 6;
 constexpr int kPvWarp = 7;
 constexpr int kStages = 2;          // KV page ring (a full page per stage)
@@ -81,7 +84,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,                   // producer (+tx) and 4 softmax warps (q in TMEM)
+    B_Q_FULL = 0,                   // producer (+tx) and the softmax warps (q in TMEM)
     B_Q_EMPTY = 1,                  // last QK of an item done, in both CTAs
     B_KV_FULL = 2,                  // + stage
     B_KV_EMPTY = B_KV_FULL + kStages,  // + stage; both CTAs' PVs done
@@ -90,8 +93,10 @@ enum : uint32_t {
     B_P_FULL = B_S_EMPTY + 1,
     B_PV_DONE = B_P_FULL + 1,
     B_O_FREE = B_PV_DONE + 1,
-    B_EPI = B_O_FREE + 1,           // 4 softmax warps done with the staged epilogue
-    B_DRAIN = B_EPI + 1,            // + issuer (0: QK a, 1: QK b, 2: PV)
+    B_EPI = B_O_FREE + 1,           // softmax warps done with the staged epilogue
+    B_PAIR = B_EPI + 1,             // + lane quarter: both halves posted their row max
+    B_PAIRL = B_PAIR + 4,           // + lane quarter: both halves posted their row sum
+    B_DRAIN = B_PAIRL + 4,          // + issuer (0: QK a, 1: QK b, 2: PV)
     B_COUNT = B_DRAIN + 3,
 };
 static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
@@ -185,18 +190,22 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(ctl, B_Q_FULL), 5);
+        mbar_init(bar(ctl, B_Q_FULL), 1 + kSoftmaxWarps);
         mbar_init(bar(ctl, B_Q_EMPTY), 2 * kClusterSize);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(ctl, B_KV_FULL + s), 1);
             mbar_init(bar(ctl, B_KV_EMPTY + s), kClusterSize);
         }
         mbar_init(bar(ctl, B_S_FULL), 2);
-        mbar_init(bar(ctl, B_S_EMPTY), 4);
-        mbar_init(bar(ctl, B_P_FULL), 4);
+        mbar_init(bar(ctl, B_S_EMPTY), kSoftmaxWarps);
+        mbar_init(bar(ctl, B_P_FULL), kSoftmaxWarps);
         mbar_init(bar(ctl, B_PV_DONE), 1);
-        mbar_init(bar(ctl, B_O_FREE), 4);
-        mbar_init(bar(ctl, B_EPI), 4);
+        mbar_init(bar(ctl, B_O_FREE), kSoftmaxWarps);
+        mbar_init(bar(ctl, B_EPI), kSoftmaxWarps);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(bar(ctl, B_PAIR + q), 2);
+            mbar_init(bar(ctl, B_PAIRL + q), 2);
+        }
         for (int d = 0; d < 3; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
         fence_mbar_init();
     }
@@ -214,6 +223,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     cluster_sync();  // the peer's barriers are initialised before any multicast targets them
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // Launched as a programmatic dependent of the planner: everything above
+    // overlaps its tail; the schedule and every input are read only after it.
+    pdl_wait_prior();
+    pdl_launch_dependents();
 
     const PlanLayout L = plan_layout(P.batch, P.s_q, P.num_units);
     const WorkItem *items = reinterpret_cast<const WorkItem *>(P.ws + L.items);
@@ -385,12 +398,18 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
+        // Two warps per TMEM lane quarter: `half` selects the 32 score columns
+        // (tokens) and the 128 output columns a warp owns.  The two halves of
+        // a row agree on the running max through a page block that is free
+        // once the scores are computed.
         const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+        const int half = warp >= 8 ? 1 : 0;
+        const int sidx = warp >= 8 ? warp - 4 : warp - 2;   // 0..7 among the softmax warps
         const int h = quarter * 32 + lane;         // head = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + kColS;
-        const uint32_t tO = tmem + lane_off + kColO;
-        const uint32_t tQ = tmem + lane_off + kColQ;
+        const uint32_t tS = tmem + lane_off + kColS + 32 * half;
+        const uint32_t tO = tmem + lane_off + kColO + 128 * half;
+        const uint32_t tQ = tmem + lane_off + kColQ + 64 * half;
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
         bool ok = true;
@@ -402,13 +421,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q dims 0-255 of this head -> TMEM (the A operand of the first 16 k-steps)
+            // q dims [128 half, 128 half + 128) of this head -> TMEM
             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
             {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    P.q_latent + ((size_t)it.row * kHeads + h) * kDl);
+                    P.q_latent + ((size_t)it.row * kHeads + h) * kDl + 128 * half);
 #pragma unroll 1
-                for (int c = 0; c < kQTDims / 64; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t q[32];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
@@ -431,45 +450,43 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
                 bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
             }
-            float m_run = NEG_INF, l_run = 0.f;
+            float m_run = NEG_INF, l_half = 0.f;
             for (int k = 0; k < n; ++k, ++g) {
                 if (!wait_warp(ctl, bar(ctl, B_S_FULL), g & 1)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tS, r0);
-                tmem_ld32(tS + 32, r1);
-                tmem_wait_ld();
-                {   // add the second partial (dims 288-575): the same order in both CTAs
+                uint32_t r[32];
+                {   // this half's columns of both partial sums (dims 0-287, 288-575)
                     uint32_t t[32];
+                    tmem_ld32(tS, r);
                     tmem_ld32(tS + 64, t);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        r0[j] = __float_as_uint(__uint_as_float(r0[j]) + __uint_as_float(t[j]));
-                    tmem_ld32(tS + 96, t);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r1[j] = __float_as_uint(__uint_as_float(r1[j]) + __uint_as_float(t[j]));
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY));
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
-                float s[64];
-                float m_loc = NEG_INF;
+                uint8_t *stage = smem + kOffStage + (g % kStages) * kStageBytes;
+                float s[32];
+                float m_half = NEG_INF;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float a = __uint_as_float(r0[j]) * P.scale_log2;
-                    float c = __uint_as_float(r1[j]) * P.scale_log2;
-                    a = j < valid ? a : NEG_INF;
-                    c = 32 + j < valid ? c : NEG_INF;
+                    float a = __uint_as_float(r[j]) * P.scale_log2;
+                    a = 32 * half + j < valid ? a : NEG_INF;
                     s[j] = a;
-                    s[32 + j] = c;
-                    m_loc = fmaxf(m_loc, fmaxf(a, c));
+                    m_half = fmaxf(m_half, a);
                 }
-                // lazy rescale of the running output
+                // row max over both halves (a block of this page the PV never reads)
+                float *pm = reinterpret_cast<float *>(stage + (rank == 0 ? 4 : 2) * kBlk);
+                pm[half * 128 + h] = m_half;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_PAIR + quarter));
+                if (!wait_warp(ctl, bar(ctl, B_PAIR + quarter), g & 1)) { ok = false; break; }
+                const float m_loc = fmaxf(m_half, pm[(1 - half) * 128 + h]);
+                // lazy rescale of the running output (the same decision in both halves)
                 float alpha = 1.f;
                 bool need = false;
                 if (k == 0) {
@@ -480,21 +497,21 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     need = true;
                 }
                 // probabilities -> bf16 (registers)
-                uint32_t pk[32];
+                uint32_t pk[16];
                 float lsum = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     const float e0 = fast_exp2(s[2 * j] - m_run);
                     const float e1 = fast_exp2(s[2 * j + 1] - m_run);
                     lsum += e0 + e1;
                     pk[j] = pack_bf16(e0, e1);
                 }
-                // PV(g-1) must be done before O is rescaled or P is overwritten
+                // PV(g-1) must be done before O is rescaled
                 if (g >= 1 && !wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) { ok = false; break; }
                 if (__any_sync(0xffffffffu, need)) {
                     tc_fence_after();
 #pragma unroll 1
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
                         tmem_ld32(tO + ch * 32, o);
                         tmem_wait_ld();
@@ -505,20 +522,21 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                     tmem_wait_st();
                 }
-                l_run = l_run * alpha + lsum;
-                {   // P row -> the stage's spare blocks, K-major with the 128-byte swizzle
-                    uint8_t *prow = smem + kOffStage + (g % kStages) * kStageBytes +
-                                    (rank == 0 ? 7 : 0) * kBlk + h * 128;
+                l_half = l_half * alpha + lsum;
+                {   // this half's 32 tokens of the P row, K-major with the 128-byte swizzle
+                    uint8_t *prow = stage + (rank == 0 ? 7 : 0) * kBlk + h * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = 4 * half + cc;
                         *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    }
                 }
                 if (valid < kPage) {
                     // zero this CTA's latent rows of the masked tail so that 0 * garbage stays 0
-                    uint8_t *vbase = smem + kOffStage + (g % kStages) * kStageBytes + 4 * rank * kBlk;
+                    uint8_t *vbase = stage + 4 * rank * kBlk;
                     const int per_blk = (kPage - valid) * 8;  // 16-byte chunks per block
-                    for (int idx = (warp - 2) * 32 + lane; idx < 4 * per_blk; idx += 128) {
+                    for (int idx = sidx * 32 + lane; idx < 4 * per_blk; idx += 32 * kSoftmaxWarps) {
                         const int blk = idx / per_blk, rem = idx % per_blk;
                         const int tok = valid + rem / 8;
                         *reinterpret_cast<uint4 *>(vbase + blk * kBlk + tok * 128 + (rem % 8) * 16) =
@@ -535,23 +553,30 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             // epilogue: wait for the last PV, normalise, store this CTA's half.  The
             // rows go through the last page's stage (free now: its QK and PV are done
             // and it is only refilled after this epilogue releases it) so that every
-            // global store writes 512 contiguous bytes of one row.
+            // global store writes 256 contiguous bytes of one row.
             if (!wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) break;
             tc_fence_after();
+            const uint32_t s_last = (g - 1) % kStages;
+            uint8_t *lstage = smem + kOffStage + s_last * kStageBytes;
+            float *pl = reinterpret_cast<float *>(lstage + 8 * kBlk);  // row sums of both halves
+            pl[half * 128 + h] = l_half;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl, B_PAIRL + quarter));
+            if (!wait_warp(ctl, bar(ctl, B_PAIRL + quarter), ii & 1)) break;
+            const float l_run = pl[h] + pl[128 + h];   // the same order in both halves
             const float nan = __int_as_float(0x7fc00000);
             const float inv = bad ? nan : 1.f / l_run;
             const float lse = bad ? nan : (m_run + log2f(l_run)) * 0.69314718055994531f;
-            const uint32_t s_last = (g - 1) % kStages;
-            uint8_t *stg = smem + kOffStage + s_last * kStageBytes + quarter * 16384;  // 32 rows x 512 B
-            uint8_t *my_stg = stg + lane * 512;
+            uint8_t *stg = lstage + sidx * 8192;     // 32 rows x 256 B
+            uint8_t *my_stg = stg + lane * 256;
             const bool final_out = it.part < 0;
-            const int passes = final_out ? 1 : 2;   // 512 B of a row per pass
+            const int passes = final_out ? 1 : 2;    // 256 B of a row per pass
 #pragma unroll 1
             for (int pass = 0; pass < passes; ++pass) {
                 // TMEM -> normalised values -> swizzled staging row (chunk c at c ^ lane)
                 if (final_out) {
 #pragma unroll 1
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
                         tmem_ld32(tO + ch * 32, o);
                         tmem_wait_ld();
@@ -563,19 +588,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
                             v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
                             const int c = ch * 4 + q;
-                            *reinterpret_cast<uint4 *>(my_stg + ((c ^ lane) << 4)) = v;
+                            *reinterpret_cast<uint4 *>(my_stg + ((c ^ (lane & 15)) << 4)) = v;
                         }
                     }
                 } else {
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < 2; ++ch) {
                         uint32_t o[32];
-                        tmem_ld32(tO + (pass * 4 + ch) * 32, o);
+                        tmem_ld32(tO + (pass * 2 + ch) * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const int c = ch * 8 + q;
-                            *reinterpret_cast<float4 *>(my_stg + ((c ^ lane) << 4)) =
+                            *reinterpret_cast<float4 *>(my_stg + ((c ^ (lane & 15)) << 4)) =
                                 make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
                                             __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
                         }
@@ -587,26 +612,29 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
                 }
                 __syncwarp();
-                // staging -> global, one row per step, 32 lanes x 16 B contiguous
+                // staging -> global: two rows per step, 16 lanes x 16 B contiguous per row
+                const int j = lane & 15;
 #pragma unroll 4
-                for (int r = 0; r < 32; ++r) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 512 + ((lane ^ r) << 4));
+                for (int st = 0; st < 16; ++st) {
+                    const int r = 2 * st + (lane >> 4);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 256 + ((j ^ (r & 15)) << 4));
                     const size_t hr = (size_t)it.row * kHeads + quarter * 32 + r;
                     if (final_out) {
-                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256)[lane] = v;
+                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256 + half * 128)[j] = v;
                     } else {
                         const size_t slot = (size_t)it.part * kHeads + quarter * 32 + r;
-                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + pass * 128)[lane] = v;
+                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + half * 128 +
+                                                  pass * 64)[j] = v;
                     }
                 }
                 __syncwarp();
             }
-            if (rank == 0) {
+            if (rank == 0 && half == 0) {
                 if (final_out) P.lse[(size_t)it.row * kHeads + h] = lse;
                 else lse_part[(size_t)it.part * kHeads + h] = lse;
             }
             if (bad && lane == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
-            // once all four softmax warps are done with the stage, release it in both CTAs
+            // once every softmax warp is done with the stage, release it in both CTAs
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
@@ -752,13 +780,15 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = kClusterSize;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterSize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, mla_main_tc_kernel, p);
 }
 

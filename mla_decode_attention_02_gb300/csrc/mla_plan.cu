@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "mla_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -86,6 +87,9 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     int32_t *row_item0 = reinterpret_cast<int32_t *>(ws + L.row_item0);
     int64_t *row_pos = reinterpret_cast<int64_t *>(ws + L.row_pos);
 
+    // The main kernel may start its prologue now; it waits for this grid before
+    // reading the schedule.
+    ptx::pdl_launch_dependents();
     // Pass 1: pages of every row and its cost-line position (exclusive prefix of costs).
     if (threadIdx.x == 0) {
         carry = 0;
