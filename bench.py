@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode KV-cache TB/s, TFLOPS and % of GB300 roofline; µs per decode step"
-NORTH_STAR_HBM_TBS = 8.0
+NOMINAL_HBM_TBS = 8.0
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MAIN_KERNEL_SRC = os.path.join(ROOT, "mla_decode_attention_02_gb300", "csrc")
@@ -475,7 +475,7 @@ def run_native(args, rank, world, local):
             "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
             "algorithmic_bytes_per_launch": cache_b, "flops_per_launch": fl,
             "launch_ms": main_ms, "hbm_frac": hbm_frac, "tensor_frac": tensor_frac}
-    t_roof = max(cache_b / (NORTH_STAR_HBM_TBS * 1e12), fl / (peaks["bf16_tflops"] * 1e12))
+    t_roof = max(cache_b / (NOMINAL_HBM_TBS * 1e12), fl / (peaks["bf16_tflops"] * 1e12))
     t_roof_meas = max(cache_b / (hbm_peak * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
 
     cpu_base = None
