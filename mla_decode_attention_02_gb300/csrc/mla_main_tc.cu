@@ -10,33 +10,37 @@
 //
 // GB300 design.  The fp32 output of one row (128 heads x 512 values =
 // 256 KB) alone fills one SM's tensor memory, so a work unit is a cluster of
-// two CTAs on two SMs, and CTA c owns output columns [256c, 256c + 256).
-// Cross-SM traffic through distributed shared memory measures only
-// 10-20 GB/s per SM on this part, far too slow to exchange per-page score
-// partials, so nothing is exchanged per page: each CTA computes the full
-// score tile itself and the pair shares only the page loads.
+// two CTAs on two SMs: CTA c owns output columns [256c, 256c + 256) and the
+// tokens [32c, 32c + 32) of every 64-token page.
 //
-//   page g (64 tokens x 576) -> TMA multicast: CTA 0 loads dim blocks 0-4,
-//                               CTA 1 blocks 5-8, each into both CTAs
-//   S   = q . k^T            tcgen05 M=128 (heads) N=64 (tokens) K=576, fp32
-//                            in TMEM, as two partial sums (dims 0-287 and
-//                            288-575) from two issuing warps; q dims 0-255
-//                            are the A operand in TMEM, 256-575 in shared memory
-//   P   = exp2(S*scale*log2e - m)    fp32 online softmax with a lazily
-//                            raised running max, rounded to bf16 into two
-//                            blocks of the page's stage that this CTA's PV
-//                            does not read
-//   O_c += P . V_c           tcgen05 M=128 N=256 K=64,
-//                            B = the page's latent dims [256c, 256c + 256)
+//   page g -> TMA: each CTA loads its own 32 tokens (all 576 dims); the
+//             dims the peer's PV needs go to both CTAs (multicast)
+//   S_c = q . k_c^T     tcgen05 M=128 (heads) N=32 (own tokens) K=576, fp32
+//                       in TMEM; q dims 0-383 are the A operand in TMEM,
+//                       384-575 in shared memory
+//   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, written into
+//                       this CTA's P tile and the peer's (st.async, 8 KB)
+//   merge: the pair agrees on the running max per head (each side's max
+//          travels with its P half; the lower half is scaled), keeps the
+//          row sum of both halves and rescales O when the max grows
+//   O_c += [P_0 | P_1] . V_c   tcgen05 M=128 N=256 K=64, V_c = the page's
+//                       latent dims [256c, 256c + 256) of all 64 tokens
 //
-// TMEM (512 columns): O half [0,256), S partials [256,384), q [384,512).
-// Warp roles per CTA: warp 0 issues TMA; warps 1 and 6 issue the two QK
-// partial sums and warp 7 the PV product (one thread issues a tcgen05.mma
-// about every 27 ns, so each chain gets its own issuer); warp 1 also owns
-// TMEM; warps 2-5 and 8-11 (two per TMEM lane quarter, one thread per head
-// and half of the columns) load q into TMEM and run the softmax and the
-// epilogue.  Every wait is bounded: on time-out the kernel
-// records MLA_DEV_TIMEOUT and winds down instead of hanging.
+// Measured on this part: one SM's shared memory streams about 250 GB/s,
+// and each page costs this layout ~200 KB of shared-memory traffic per SM
+// (ingest 52 KB, score operands 84 KB, PV operands 48 KB, P 16 KB) against
+// ~290 KB when each CTA scores the whole page; distributed shared memory
+// moves only 15-20 GB/s per SM, which the 8 KB P half per page fits.
+//
+// TMEM (512 columns): O half [0,256), S (two pages) [256,320), q [320,512).
+// Warp roles per CTA: warp 0 issues TMA; warps 1 and 2 issue the score
+// products of even and odd pages and warp 3 the PV product (each a whole
+// warp that waits together and issues from one elected lane: about 15 ns per
+// tcgen05.mma, against 35 ns from a lane-0 branch); warps 4-7 (one per TMEM
+// lane quarter, one thread per head) load q into TMEM and compute P; warps
+// 8-11 merge the two halves and run the epilogue.  Every wait is bounded: on
+// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
+// hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,59 +56,89 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;       // warp 0 TMA, warps 1/6 QK MMA, 7 PV MMA, 2-5 + 8-11 softmax
-constexpr int kSoftmaxWarps = 8;    // two per TMEM lane quarter, 32 score columns each
-constexpr int kQkbWarp = 6;
-constexpr int kPvWarp = 7;
-constexpr int kStages = 2;          // KV page ring (a full page per stage)
-constexpr int kPrefetch = 2;        // L2 prefetch distance in pages (one beyond the stages)
+constexpr int kThreads = 384;
+constexpr int kQkWarp0 = 1;         // warps 1, 2: score MMAs of even, odd pages
+constexpr int kPvWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;    // warps 4-7
+constexpr int kMergeWarp0 = 8;      // warps 8-11
+constexpr int kStages = 3;          // KV page ring
+constexpr int kPrefetch = 3;        // L2 prefetch distance in pages
 constexpr int kClusterSize = 2;
-constexpr uint16_t kBoth = 0x3;     // multicast mask: both CTAs of the pair
-constexpr uint32_t kBlk = 64 * 128;               // page block: 64 tokens x 64 dims (SW128)
-constexpr uint32_t kStageBytes = 9 * kBlk;        // dims 0-511 latent + 512-575 rope
-constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims (SW128)
-constexpr uint32_t kQSBytes = 5 * kQBlk;          // q dims 256-575 in shared memory
-constexpr int kQTDims = 256;                      // q dims 0-255 live in TMEM
+constexpr uint16_t kBoth = 0x3;
+constexpr int kHalfTok = 32;                      // tokens of a page per CTA
+constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-byte swizzle
+constexpr uint32_t kStageBytes = 13 * kBox;       // 13 boxes land in each CTA per page
+constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
+constexpr int kQTDims = 384;                      // q dims 0-383 live in TMEM
+constexpr uint32_t kQSBytes = 3 * kQBlk;          // q dims 384-575 in shared memory
 constexpr uint32_t kOffQS = 0;
 constexpr uint32_t kOffStage = kQSBytes;
-constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+constexpr uint32_t kOffRef = kOffStage + kStages * kStageBytes;  // merge state, see kRef*
+constexpr uint32_t kRefMax = 0;       // agreed max per head after each page, 2 (page parity) x 128
+constexpr uint32_t kRefFinal = 1024;  // (row sum, max) per head at an item's end, 128 x float2
+constexpr uint32_t kRefOld = 2048;    // agreed max before a page that needs a fix, 128 floats
+constexpr uint32_t kRefCmd = 2560;    // command to the merge warps: type, stage, item page, page
+constexpr uint32_t kOffBar = kOffRef + 4096;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers, + alignment slack
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
+// Stage layout (4 KB slots).  Rank r loads its own token half (tokens 32r..)
+// of all nine 64-dim blocks; the four blocks holding the peer's output dims
+// are multicast, so both CTAs see them at the same offset.
+//   slots 4r..4r+3   own tokens, the peer's output dims: score operand only,
+//                    then this CTA's P tile (128 heads x 64 tokens, bf16)
+//   slots 4(1-r)..   the peer's tokens, this CTA's output dims (PV operand)
+//   slots 8-11       own tokens, this CTA's output dims (score + PV operand)
+//   slot 12          own tokens, rope dims (score operand only), then the
+//                    two halves' (max, row sum) per head, 1 KB per CTA
+constexpr uint32_t kSlotOwnV = 8;
+constexpr uint32_t kSlotRope = 12;
+constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, sum)
+
+__host__ __device__ constexpr uint32_t own_slot(uint32_t rank, uint32_t blk) {
+    return blk == 8 ? kSlotRope : (blk / 4 == rank ? kSlotOwnV + blk % 4 : 4 * rank + blk % 4);
+}
+
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
-constexpr uint32_t kColS = 256;     // 2 x 64 fp32 partial scores (dims 0-287, 288-575)
-constexpr uint32_t kColQ = 384;     // 128 columns of packed bf16 q (dims 0-255)
+constexpr uint32_t kColS = 256;     // 2 x 32 fp32 scores (pages of even / odd index)
+constexpr uint32_t kColQ = 320;     // 192 columns of packed bf16 q (dims 0-383)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: raise the max only when it grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,                   // producer (+tx) and the softmax warps (q in TMEM)
-    B_Q_EMPTY = 1,                  // last QK of an item done, in both CTAs
-    B_KV_FULL = 2,                  // + stage
-    B_KV_EMPTY = B_KV_FULL + kStages,  // + stage; both CTAs' PVs done
-    B_S_FULL = B_KV_EMPTY + kStages,
-    B_S_EMPTY = B_S_FULL + 1,
-    B_P_FULL = B_S_EMPTY + 1,
-    B_PV_DONE = B_P_FULL + 1,
-    B_O_FREE = B_PV_DONE + 1,
-    B_EPI = B_O_FREE + 1,           // softmax warps done with the staged epilogue
-    B_PAIR = B_EPI + 1,             // + lane quarter: both halves posted their row max
-    B_PAIRL = B_PAIR + 4,           // + lane quarter: both halves posted their row sum
-    B_DRAIN = B_PAIRL + 4,          // + issuer (0: QK a, 1: QK b, 2: PV)
+    B_Q_FULL = 0,                        // producer (+tx), softmax and merge warps (q in TMEM)
+    B_Q_EMPTY = 1,                       // both score issuers of both CTAs done with q
+    B_FULL = 2,                          // + stage: dim blocks 0-5 of the page landed (+tx)
+    B_FULLB = B_FULL + kStages,          // + stage: the rest landed (+tx)
+    B_EMPTY_OWN = B_FULLB + kStages,     // + stage: this CTA's PV done with the stage
+    B_EMPTY_PEER = B_EMPTY_OWN + kStages,  // + stage: the peer's PV done with its copy
+    B_SFULL = B_EMPTY_PEER + kStages,    // + page parity: scores in TMEM
+    B_QKP = B_SFULL + 2,                 // + page parity: the peer's scores done
+    B_SEMPTY = B_QKP + 2,                // + page parity: scores read and the peer's seen, both CTAs
+    B_SDONE = B_SEMPTY + 2,              // + stage: own P half written
+    B_PMSG = B_SDONE + kStages,          // + stage: the peer's P half arrived (+tx)
+    B_RESDONE = B_PMSG + kStages,        // + page parity: agreed max published
+    B_PVDONE = B_RESDONE + 2,            // + page parity: PV done
+    B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
+    B_OFREE = B_PVLAST + 1,              // epilogue done reading O
+    B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
+    B_CMD = B_EPI + 1,                   // PV warp -> merge warps: a fix or an item's end
+    B_FIXED = B_CMD + 1,                 // merge warps -> PV warp: fix done
+    B_DRAIN = B_FIXED + 1,               // + issuer (0, 1: score, 2: PV)
     B_COUNT = B_DRAIN + 3,
 };
-static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
+static_assert(B_COUNT * 8 <= 512, "barrier area");
 
 struct Params {
     CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
     CUtensorMap tm_q_rope;  // q_rope   as [rows*128][64],  box 64 x 128, SW128
-    CUtensorMap tm_kv;      // kv_cache as [pages][64][576], box 64 x 64 x 1, SW128
+    CUtensorMap tm_kv;      // kv_cache as [pages][64][576], box 64 x 32 x 1, SW128
     const __nv_bfloat16 *q_latent;
     const int32_t *block_table;
     uint8_t *ws;
@@ -130,13 +164,25 @@ __device__ __forceinline__ void fail(const Ctl &c) {
     }
 }
 
+// How a wait acquires: CTA scope; cluster scope, for phases that the peer
+// CTA completes with data (st.async, TMA multicast, its MMAs' commits); or
+// not at all, for pure progress signals from the peer.
+enum Scope : int { kCta = 0, kCluster = 1, kSignal = 2 };
+
+__device__ __forceinline__ bool try_wait(uint32_t b, uint32_t parity, int scope) {
+    return scope == kCta       ? mbar_try_wait(b, parity)
+           : scope == kCluster ? mbar_try_wait_cluster(b, parity)
+                               : mbar_try_wait_relaxed_cluster(b, parity);
+}
+
 // Bounded wait for the completion of the phase with the given parity: gives
 // up (and flags the time-out) after kWaitLimitNs, or at once if another
 // thread of the CTA already gave up.
-__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity) {
+__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
+                                     int scope = kCta) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(b, parity)) return true;
+        if (try_wait(b, parity, scope)) return true;
         if ((i & 255) == 255) {
             if (*c.abort) return false;
             const uint64_t t = globaltimer_ns();
@@ -152,8 +198,9 @@ __device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity) 
 
 // Warp-uniform version: every lane waits (and acquires), and the warp agrees
 // on the outcome, so no lane leaves a .sync.aligned sequence early.
-__device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait(c, b, parity));
+__device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity,
+                                          int scope = kCta) {
+    return __all_sync(0xffffffffu, wait(c, b, parity, scope));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -167,6 +214,46 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Scale the four 16-byte chunks of one P row half (bf16) by f.
+__device__ __forceinline__ void scale_p_half(uint8_t *prow, int h, int half, float f) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        uint4 *p = reinterpret_cast<uint4 *>(prow + (((4 * half + cc) ^ (h & 7)) << 4));
+        uint4 v = *p;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&w[e]);
+            const float2 fx = __bfloat1622float2(x);
+            w[e] = pack_bf16(fx.x * f, fx.y * f);
+        }
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// q dims [192 part, 192 part + 192) of one head -> TMEM (96 columns).  All
+// 24 loads are in flight before the first store, so an item's q costs one
+// memory round trip rather than one per 64 dims.
+__device__ __forceinline__ void load_q_part(const __nv_bfloat16 *q_row, uint32_t tq, int part) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(q_row) + part * 24;
+    uint4 x[24];
+#pragma unroll
+    for (int v = 0; v < 24; ++v) x[v] = src[v];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        uint32_t q[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            q[4 * v] = x[c * 8 + v].x;
+            q[4 * v + 1] = x[c * 8 + v].y;
+            q[4 * v + 2] = x[c * 8 + v].z;
+            q[4 * v + 3] = x[c * 8 + v].w;
+        }
+        tmem_st32(tq + (part * 3 + c) * 32, q);
+    }
+    tmem_wait_st();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 mla_main_tc_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
@@ -175,11 +262,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     const uint32_t s_base = smem_u32(smem);
     const uint32_t s_qs = s_base + kOffQS;
     const uint32_t s_stage = s_base + kOffStage;
+    float *oref = reinterpret_cast<float *>(smem + kOffRef);  // [page parity][head]
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const uint16_t peer_mask = (uint16_t)(1u << peer);
     const uint32_t unit = cluster_id_x();
 
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(P.ws);
@@ -190,22 +280,29 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(ctl, B_Q_FULL), 1 + kSoftmaxWarps);
+        mbar_init(bar(ctl, B_Q_FULL), 1 + 8);
         mbar_init(bar(ctl, B_Q_EMPTY), 2 * kClusterSize);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(ctl, B_KV_FULL + s), 1);
-            mbar_init(bar(ctl, B_KV_EMPTY + s), kClusterSize);
+            mbar_init(bar(ctl, B_FULL + s), 1);
+            mbar_init(bar(ctl, B_FULLB + s), 1);
+            mbar_init(bar(ctl, B_EMPTY_OWN + s), 1);
+            mbar_init(bar(ctl, B_EMPTY_PEER + s), 1);
+            mbar_init(bar(ctl, B_SDONE + s), 4);
+            mbar_init(bar(ctl, B_PMSG + s), 128);
         }
-        mbar_init(bar(ctl, B_S_FULL), 2);
-        mbar_init(bar(ctl, B_S_EMPTY), kSoftmaxWarps);
-        mbar_init(bar(ctl, B_P_FULL), kSoftmaxWarps);
-        mbar_init(bar(ctl, B_PV_DONE), 1);
-        mbar_init(bar(ctl, B_O_FREE), kSoftmaxWarps);
-        mbar_init(bar(ctl, B_EPI), kSoftmaxWarps);
-        for (int q = 0; q < 4; ++q) {
-            mbar_init(bar(ctl, B_PAIR + q), 2);
-            mbar_init(bar(ctl, B_PAIRL + q), 2);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bar(ctl, B_SFULL + p), 1);
+            mbar_init(bar(ctl, B_QKP + p), 1);
+            mbar_init(bar(ctl, B_SEMPTY + p), 2 * 4);
+            mbar_init(bar(ctl, B_RESDONE + p), 1);
         }
+        mbar_init(bar(ctl, B_PVDONE), 1);
+        mbar_init(bar(ctl, B_PVDONE + 1), 1);
+        mbar_init(bar(ctl, B_PVLAST), 1);
+        mbar_init(bar(ctl, B_OFREE), 4);
+        mbar_init(bar(ctl, B_EPI), 4);
+        mbar_init(bar(ctl, B_CMD), 1);
+        mbar_init(bar(ctl, B_FIXED), 4);
         for (int d = 0; d < 3; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
         fence_mbar_init();
     }
@@ -214,7 +311,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         prefetch_tmap(&P.tm_q_rope);
         prefetch_tmap(&P.tm_kv);
     }
-    if (warp == 1) {
+    if (warp == kQkWarp0) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -247,15 +344,15 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         uint32_t g = 0;
-        for (int i = i_begin; i < i_end && !abort_flag; ++i) {
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
             const int b = it.row / P.s_q;
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            bool ok = true;
-            const int kb0 = rank == 0 ? 0 : 5, kb1 = rank == 0 ? 5 : 9;  // this CTA's page blocks
             const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
+            const int tok0 = kHalfTok * (int)rank;
             for (int k0 = 0; k0 < n && ok; k0 += 32) {
                 const int mine = k0 + lane < n ? bt[k0 + lane] : 0;
                 const int ahead = k0 + lane + kPrefetch < n ? bt[k0 + lane + kPrefetch] : 0;
@@ -264,25 +361,42 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const int page = __shfl_sync(0xffffffffu, mine, kk);
                     const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
                     const uint32_t s = g % kStages;
-                    // the stage is free in both CTAs (our loads write into both)
-                    if (g >= kStages &&
-                        !wait_warp(ctl, bar(ctl, B_KV_EMPTY + s), ((g / kStages) - 1) & 1)) {
-                        ok = false;
-                        break;
+                    // our loads write into both CTAs: both copies of the stage must be free
+                    if (g >= kStages) {
+                        const uint32_t par = ((g / kStages) - 1) & 1;
+                        if (!wait_warp(ctl, bar(ctl, B_EMPTY_OWN + s), par) ||
+                            !wait_warp(ctl, bar(ctl, B_EMPTY_PEER + s), par, kSignal)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     if (lane == 0) {
-                        const uint32_t fb = bar(ctl, B_KV_FULL + s);
+                        // Blocks 0-5 (the score MMAs with q in TMEM) and 6-8 complete
+                        // separate barriers, so that those MMAs start before the rest
+                        // lands.  A multicast block completes the same barrier in both
+                        // CTAs: group A here also receives the peer's blocks 4r..4r+3
+                        // that lie below 6.
+                        const uint32_t fa = bar(ctl, B_FULL + s), fb = bar(ctl, B_FULLB + s);
                         const uint32_t dst = s_stage + s * kStageBytes;
-                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        const uint32_t bytes_a = (6 + (rank == 0 ? 4 : 2)) * kBox;
+                        mbar_arrive_expect_tx(fa, bytes_a);
+                        mbar_arrive_expect_tx(fb, kStageBytes - bytes_a);
                         // An out-of-pool page index reads zeros (TMA bounds fill);
-                        // the softmax warps flag the row.
-                        for (int kb = kb0; kb < kb1; ++kb)
-                            tma_load_3d_mc(dst + kb * kBlk, &P.tm_kv, 64 * kb, 0, page, fb, kBoth);
+                        // the merge warps flag the row.
+#pragma unroll
+                        for (uint32_t blk = 0; blk < 9; ++blk) {
+                            const uint32_t d = dst + own_slot(rank, blk) * kBox;
+                            const uint32_t fbar = blk < 6 ? fa : fb;
+                            if (blk < 8 && blk / 4 != rank)
+                                tma_load_3d_mc(d, &P.tm_kv, 64 * blk, tok0, page, fbar, kBoth);
+                            else
+                                tma_load_3d(d, &P.tm_kv, 64 * blk, tok0, page, fbar);
+                        }
                     }
                     if (k0 + kk == 0) {
-                        // q dims 256-575, once the first page is on its way: both CTAs'
-                        // copies must be free (last QKs of the previous item done)
-                        if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) {
+                        // q dims 384-575, once the first page is on its way: both CTAs'
+                        // copies must be free (last score MMAs of the previous item done)
+                        if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
                             ok = false;
                             break;
                         }
@@ -290,105 +404,199 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             const uint32_t fb = bar(ctl, B_Q_FULL);
                             mbar_arrive_expect_tx(fb, kQSBytes);
                             const int y = it.row * kHeads;
-                            for (int j = rank == 0 ? 0 : 3; j < (rank == 0 ? 3 : 5); ++j) {
-                                if (j < 4)
-                                    tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_lat, kQTDims + 64 * j, y,
-                                                   fb, kBoth);
-                                else
-                                    tma_load_2d_mc(s_qs + j * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                            if (rank == 0) {
+                                tma_load_2d_mc(s_qs, &P.tm_q_lat, kQTDims, y, fb, kBoth);
+                                tma_load_2d_mc(s_qs + kQBlk, &P.tm_q_lat, kQTDims + 64, y, fb, kBoth);
+                            } else {
+                                tma_load_2d_mc(s_qs + 2 * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
                             }
                         }
                     }
-                    // warm L2 for a page beyond the two stages in flight
+                    // warm L2 for a page beyond the stages in flight
                     if (lane == 0 && k0 + kk + kPrefetch < n)
-                        for (int kb = kb0; kb < kb1; ++kb)
-                            tma_prefetch_3d(&P.tm_kv, 64 * kb, 0, page_ahead);
+                        for (int blk = 0; blk < 9; ++blk)
+                            tma_prefetch_3d(&P.tm_kv, 64 * blk, tok0, page_ahead);
                     __syncwarp();
                 }
             }
-            if (!ok) break;
         }
-    } else if (warp == 1 || warp == kQkbWarp || warp == kPvWarp) {
+    } else if (warp == kQkWarp0 || warp == kQkWarp0 + 1 || warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuers
-        // One thread issues a tcgen05.mma about every 27 ns, so the score
-        // contraction is split over two issuers with separate accumulators
-        // (dims 0-287 and 288-575, summed by the softmax in a fixed order)
-        // and the PV product gets a third.
-        if (lane == 0) {
-            const int role = warp == 1 ? 0 : (warp == kQkbWarp ? 1 : 2);
-            // Descriptor bases; every MMA below adds a compile-time byte offset (>> 4).
-            const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
-            const uint64_t d_kv0 = smem_desc(s_stage, 16, 1024, 2);
-            const uint64_t d_v0 = smem_desc(s_stage + 4 * rank * kBlk, 8192, 1024, 2);
-            const uint64_t d_p0 = smem_desc(s_stage + (rank == 0 ? 7 : 0) * kBlk, 16, 1024, 2);
-            constexpr uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
-            constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
-            const uint32_t tSa = tmem + kColS, tSb = tmem + kColS + 64, tQ = tmem + kColQ;
-            const uint32_t tO = tmem + kColO;
-            uint32_t g = 0;
-            bool ok = true;
-            for (int i = i_begin; i < i_end && ok; ++i) {
-                const WorkItem it = items[i];
-                const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
-                const uint32_t ii = (uint32_t)(i - i_begin);
-                if (role < 2 && !wait(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
-                for (int k = 0; k < n && ok; ++k, ++g) {
-                    const uint32_t s = g % kStages;
-                    const uint64_t stage_off = (uint64_t)((s * kStageBytes) >> 4);
-                    if (role < 2) {
-                        if (!wait(ctl, bar(ctl, B_KV_FULL + s), (g / kStages) & 1)) { ok = false; break; }
-                        if (g >= 1 && !wait(ctl, bar(ctl, B_S_EMPTY), (g - 1) & 1)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t kv = d_kv0 + stage_off;
-                        if (role == 0) {
-                            // S_a: dims 0-255 (q from TMEM) and 256-287 (q block 0, k-steps 0-1)
+        // The whole warp runs the schedule and waits; one elected lane issues.
+        const int role = warp - kQkWarp0;   // 0, 1: score MMAs of even / odd pages; 2: PV
+        uint32_t slot_off[9];
 #pragma unroll
-                            for (int ks = 0; ks < 16; ++ks)
-                                mma_ts(tSa, tQ + 8 * ks,
-                                       kv + (uint64_t)(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4),
-                                       id_qk, ks > 0 ? 1u : 0u);
-#pragma unroll
-                            for (int ks = 0; ks < 2; ++ks)
-                                mma_ss(tSa, d_qs + (uint64_t)((ks * 32) >> 4),
-                                       kv + (uint64_t)((4 * kBlk + ks * 32) >> 4), id_qk, 1u);
-                        } else {
-                            // S_b: dims 288-319 (q block 0, k-steps 2-3) and 320-575 (q blocks 1-4)
-#pragma unroll
-                            for (int ks = 2; ks < 4; ++ks)
-                                mma_ss(tSb, d_qs + (uint64_t)((ks * 32) >> 4),
-                                       kv + (uint64_t)((4 * kBlk + ks * 32) >> 4), id_qk,
-                                       ks > 2 ? 1u : 0u);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                mma_ss(tSb,
-                                       d_qs + (uint64_t)(((1 + (j >> 2)) * kQBlk + (j & 3) * 32) >> 4),
-                                       kv + (uint64_t)(((5 + (j >> 2)) * kBlk + (j & 3) * 32) >> 4),
-                                       id_qk, 1u);
-                        }
-                        mma_commit(bar(ctl, B_S_FULL));
-                        if (k == n - 1) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
-                    } else {
-                        // O_c (+)= P . V_c, P (bf16) in two spare blocks of the page's stage
-                        if (!wait(ctl, bar(ctl, B_P_FULL), g & 1)) { ok = false; break; }
-                        if (k == 0 && ii > 0 && !wait(ctl, bar(ctl, B_O_FREE), (ii - 1) & 1)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t v = d_v0 + stage_off;
-                        const uint64_t pa = d_p0 + stage_off;
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tO, pa + (uint64_t)((ks * 32) >> 4), v + (uint64_t)((ks * 2048) >> 4),
-                                   id_pv, (k == 0 && ks == 0) ? 0u : 1u);
-                        mma_commit(bar(ctl, B_PV_DONE));
-                        // the last page's stage is released by the epilogue, which stages
-                        // the output through it
-                        if (k != n - 1) mma_commit_mc(bar(ctl, B_KV_EMPTY + s), kBoth);
+        for (uint32_t blk = 0; blk < 9; ++blk) slot_off[blk] = own_slot(rank, blk) * kBox;
+        // Descriptor bases; every MMA below adds a byte offset (>> 4).
+        const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
+        const uint64_t d_st = smem_desc(s_stage, 16, 1024, 2);
+        const uint64_t d_p = smem_desc(s_stage + 4 * rank * kBox, 16, 1024, 2);
+        const uint64_t d_vown = smem_desc(s_stage + kSlotOwnV * kBox, 4096, 1024, 2);
+        const uint64_t d_vpeer = smem_desc(s_stage + 4 * peer * kBox, 4096, 1024, 2);
+        constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
+        constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+        const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
+        float m_ref[4], l_sum[4];   // PV warp: agreed max and row sum of heads 4 lane..+3
+        uint32_t n_fix = 0;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const WorkItem it = items[i];
+            const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+            const uint32_t ii = (uint32_t)(i - i_begin);
+            // every score issuer takes part in every item's q hand-over, pages or not
+            if (role < 2 && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+            for (int k = 0; k < n && ok; ++k, ++g) {
+                const uint32_t s = g % kStages;
+                const uint32_t so = s * kStageBytes;
+                if (role < 2) {
+                    if ((int)(g & 1) != role) continue;
+                    if (!wait_warp(ctl, bar(ctl, B_FULL + s), (g / kStages) & 1)) { ok = false; break; }
+                    if (g >= 2 &&
+                        !wait_warp(ctl, bar(ctl, B_SEMPTY + role), ((g >> 1) - 1) & 1, kSignal)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t tS = tmem + kColS + kHalfTok * role;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 24; ++ks)
+                            mma_ts(tS, tQ + 8 * ks,
+                                   d_st + (uint64_t)((so + slot_off[ks >> 2] + (ks & 3) * 32) >> 4),
+                                   id_qk, ks > 0 ? 1u : 0u);
+                    }
+                    __syncwarp();
+                    if (!wait_warp(ctl, bar(ctl, B_FULLB + s), (g / kStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 24; ks < 36; ++ks)
+                            mma_ss(tS, d_qs + (uint64_t)((((ks - 24) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
+                                   d_st + (uint64_t)((so + slot_off[ks >> 2] + (ks & 3) * 32) >> 4),
+                                   id_qk, 1u);
+                        mma_commit(bar(ctl, B_SFULL + role));
+                        mma_commit_mc(bar(ctl, B_QKP + role), peer_mask);
+                    }
+                    __syncwarp();
+                } else {
+                    // Merge the pair's halves of page g (each lane: heads 4 lane..+3),
+                    // then O_c (+)= [P_0 | P_1] . V_c.  Usually both halves used the
+                    // agreed max and nothing changes; otherwise the merge warps scale
+                    // the lower half's P rows (and O when the max grew) first.
+                    if (!wait_warp(ctl, bar(ctl, B_SDONE + s), (g / kStages) & 1) ||
+                        !wait_warp(ctl, bar(ctl, B_PMSG + s), (g / kStages) & 1, kCluster)) {
+                        ok = false;
+                        break;
+                    }
+                    if (k == 0 && ii > 0 && !wait_warp(ctl, bar(ctl, B_OFREE), (ii - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (k == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            m_ref[j] = -INFINITY;
+                            l_sum[j] = 0.f;
+                        }
+                    }
+                    const uint8_t *msg = smem + kOffStage + so + kSlotRope * kBox + lane * 32;
+                    float m0[4], m1[4], r0[4], r1[4], nref[4];
+                    {
+                        const float4 a0 = reinterpret_cast<const float4 *>(msg)[0];
+                        const float4 a1 = reinterpret_cast<const float4 *>(msg)[1];
+                        const float4 b0 = reinterpret_cast<const float4 *>(msg + 1024)[0];
+                        const float4 b1 = reinterpret_cast<const float4 *>(msg + 1024)[1];
+                        m0[0] = a0.x; r0[0] = a0.y; m0[1] = a0.z; r0[1] = a0.w;
+                        m0[2] = a1.x; r0[2] = a1.y; m0[3] = a1.z; r0[3] = a1.w;
+                        m1[0] = b0.x; r1[0] = b0.y; m1[1] = b0.z; r1[1] = b0.w;
+                        m1[2] = b1.x; r1[2] = b1.y; m1[3] = b1.z; r1[3] = b1.w;
+                    }
+                    bool fix = false;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        nref[j] = fmaxf(m_ref[j], fmaxf(m0[j], m1[j]));   // finite: token 0 is valid
+                        fix |= (m0[j] != -INFINITY && m0[j] < nref[j]) ||
+                               (m1[j] != -INFINITY && m1[j] < nref[j]) || (k > 0 && nref[j] > m_ref[j]);
+                    }
+                    if (__any_sync(0xffffffffu, fix)) {
+                        // hand the page to the merge warps (they recompute the same factors)
+                        float *old = reinterpret_cast<float *>(smem + kOffRef + kRefOld);
+                        reinterpret_cast<float4 *>(old)[lane] = make_float4(m_ref[0], m_ref[1], m_ref[2], m_ref[3]);
+                        __threadfence_block();
+                        if (lane == 0) {
+                            int *cmd = reinterpret_cast<int *>(smem + kOffRef + kRefCmd);
+                            cmd[0] = 1;
+                            cmd[1] = (int)s;
+                            cmd[2] = k;
+                            cmd[3] = (int)g;
+                        }
+                        __syncwarp();
+                        if (elect_one()) mbar_arrive(bar(ctl, B_CMD));
+                        if (!wait_warp(ctl, bar(ctl, B_FIXED), n_fix & 1)) { ok = false; break; }
+                        ++n_fix;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float f0 = m0[j] == -INFINITY ? 0.f : (m0[j] == nref[j] ? 1.f : fast_exp2(m0[j] - nref[j]));
+                        const float f1 = m1[j] == -INFINITY ? 0.f : (m1[j] == nref[j] ? 1.f : fast_exp2(m1[j] - nref[j]));
+                        const float alpha = m_ref[j] == -INFINITY ? 0.f
+                                            : (nref[j] > m_ref[j] ? fast_exp2(m_ref[j] - nref[j]) : 1.f);
+                        l_sum[j] = l_sum[j] * alpha + r0[j] * f0 + r1[j] * f1;   // same order in both CTAs
+                        m_ref[j] = nref[j];
+                    }
+                    // the agreed max after page g, for the softmax of page g + 2
+                    float *mref = reinterpret_cast<float *>(smem + kOffRef + kRefMax);
+                    reinterpret_cast<float4 *>(mref + (g & 1) * 128)[lane] =
+                        make_float4(m_ref[0], m_ref[1], m_ref[2], m_ref[3]);
+                    if (k == n - 1) {
+                        float4 *fin = reinterpret_cast<float4 *>(smem + kOffRef + kRefFinal);
+                        fin[2 * lane] = make_float4(l_sum[0], m_ref[0], l_sum[1], m_ref[1]);
+                        fin[2 * lane + 1] = make_float4(l_sum[2], m_ref[2], l_sum[3], m_ref[3]);
+                    }
+                    __threadfence_block();
+                    __syncwarp();
+                    if (elect_one()) {
+                        mbar_arrive(bar(ctl, B_RESDONE + (g & 1)));
+                        if (k == n - 1) {   // the item's end: the merge warps run the epilogue
+                            int *cmd = reinterpret_cast<int *>(smem + kOffRef + kRefCmd);
+                            cmd[0] = 2;
+                            mbar_arrive(bar(ctl, B_CMD));
+                        }
+                    }
+                    // P halves (generic stores here and st.async from the peer) -> tensor cores
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    tc_fence_after();
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t vb = (uint32_t)(ks >> 1) == rank ? d_vown : d_vpeer;
+                            mma_ss(tO, d_p + (uint64_t)((so + ks * 32) >> 4),
+                                   vb + (uint64_t)((so + (ks & 1) * 2048) >> 4), id_pv,
+                                   (k == 0 && ks == 0) ? 0u : 1u);
+                        }
+                        mma_commit(bar(ctl, B_PVDONE + (g & 1)));
+                        // the last page's stage is released by the epilogue, which
+                        // stages the output through it
+                        if (k != n - 1) {
+                            mma_commit(bar(ctl, B_EMPTY_OWN + s));
+                            mma_commit_mc(bar(ctl, B_EMPTY_PEER + s), peer_mask);
+                        } else {
+                            mma_commit(bar(ctl, B_PVLAST));
+                        }
+                    }
+                    __syncwarp();
                 }
             }
-            // wind down: every MMA this thread issued completes before TMEM is freed
+            // this issuer is done with the item's q (in both CTAs' copies)
+            if (ok && role < 2) {
+                if (elect_one()) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
+                __syncwarp();
+            }
+        }
+        // wind down: every MMA this warp issued completes before TMEM is freed
+        if (elect_one()) {
             const uint32_t drain = bar(ctl, B_DRAIN + role);
             mma_commit(drain);
             const uint64_t t0 = globaltimer_ns();
@@ -396,50 +604,138 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= kSoftmaxWarp0 && warp < kMergeWarp0) {
         // ------------------------------------------------------------ softmax warps
-        // Two warps per TMEM lane quarter: `half` selects the 32 score columns
-        // (tokens) and the 128 output columns a warp owns.  The two halves of
-        // a row agree on the running max through a page block that is free
-        // once the scores are computed.
-        const int quarter = warp & 3;              // TMEM lane quarter this warp may access
-        const int half = warp >= 8 ? 1 : 0;
-        const int sidx = warp >= 8 ? warp - 4 : warp - 2;   // 0..7 among the softmax warps
-        const int h = quarter * 32 + lane;         // head = TMEM lane
+        // One thread per head (TMEM lane); this CTA's 32 tokens of each page.
+        const int quarter = warp & 3;
+        const int h = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + kColS + 32 * half;
-        const uint32_t tO = tmem + lane_off + kColO + 128 * half;
-        const uint32_t tQ = tmem + lane_off + kColQ + 64 * half;
+        const uint32_t tQ = tmem + lane_off + kColQ;
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const WorkItem it = items[i];
+            const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+            const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
+            const uint32_t ii = (uint32_t)(i - i_begin);
+
+            // q dims 0-191 of this head -> TMEM (the previous item's scores are
+            // done); the merge warps load dims 192-383
+            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) break;
+            load_q_part(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tQ, 0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
+            float m_prev = NEG_INF;   // max used for this half's previous page
+            for (int k = 0; k < n; ++k, ++g) {
+                const uint32_t par = g & 1, s = g % kStages;
+                // Start from the pair's agreed max of two pages back (a fixed point
+                // in the schedule, so the result does not depend on timing).  The
+                // wait is taken on every page so that no phase of the barrier is
+                // skipped.
+                float base = m_prev;
+                if (g >= 2) {
+                    if (!wait_warp(ctl, bar(ctl, B_RESDONE + par), ((g >> 1) - 1) & 1)) { ok = false; break; }
+                    if (k >= 2) base = fmaxf(base, oref[par * 128 + h]);
+                }
+                if (!wait_warp(ctl, bar(ctl, B_SFULL + par), (g >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + kColS + kHalfTok * par, r);
+                tmem_wait_ld();
+
+                const int valid = (k == n - 1) ? valid_last : kPage;
+                const int v_own = min(max(valid - kHalfTok * (int)rank, 0), kHalfTok);
+                float lm = NEG_INF;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = j < v_own ? __uint_as_float(r[j]) * P.scale_log2 : NEG_INF;
+                    r[j] = __float_as_uint(a);
+                    lm = fmaxf(lm, a);
+                }
+                // raise the max only when this half's page exceeds it by > 2^8
+                const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
+                m_prev = m_used;
+                const float mu = m_used == NEG_INF ? 0.f : m_used;
+                uint32_t pk[16];
+                float rsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float e0 = fast_exp2(__uint_as_float(r[2 * j]) - mu);
+                    const float e1 = fast_exp2(__uint_as_float(r[2 * j + 1]) - mu);
+                    rsum += e0 + e1;
+                    pk[j] = pack_bf16(e0, e1);
+                }
+                // P half -> this CTA's P tile and the peer's (once the peer's scores,
+                // which read those slots, are done), with (max, row sum)
+                if (!wait_warp(ctl, bar(ctl, B_QKP + par), (g >> 1) & 1, kSignal)) { ok = false; break; }
+                // The score buffer is released in both CTAs only now: the peer's
+                // scores of page g + 2 (which complete the next phase of this
+                // parity's QKP barrier) wait for it, so no phase is skipped.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(ctl, B_SEMPTY + par));
+                    mbar_arrive_cluster_relaxed(mapa(bar(ctl, B_SEMPTY + par), peer));
+                }
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                const uint32_t s_stg = s_stage + s * kStageBytes;
+                const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + s), peer);
+                mbar_arrive_expect_tx(bar(ctl, B_PMSG + s), kMsgBytes);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t off = h * 128 + ((((4 * rank + cc) ^ (h & 7))) << 4);
+                    const uint4 v = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    *reinterpret_cast<uint4 *>(stage + 4 * rank * kBox + off) = v;
+                    st_async_v4_b32(mapa(s_stg + 4 * peer * kBox + off, peer), v, pmsg_peer);
+                }
+                {
+                    const uint32_t off = kSlotRope * kBox + rank * 1024 + h * 8;
+                    *reinterpret_cast<float2 *>(stage + off) = make_float2(m_used, rsum);
+                    st_async_v2_f32(mapa(s_stg + off, peer), m_used, rsum, pmsg_peer);
+                }
+                if (valid < kPage) {
+                    // zero this CTA's latent rows of the masked tail (own and peer tokens)
+                    // so that 0 * garbage stays 0 in PV
+                    const int v_peer = min(max(valid - kHalfTok * (int)peer, 0), kHalfTok);
+                    const int n_own = (kHalfTok - v_own) * 8 * 4, n_peer = (kHalfTok - v_peer) * 8 * 4;
+                    for (int idx = h; idx < n_own + n_peer; idx += 128) {
+                        const bool o = idx < n_own;
+                        const int x = o ? idx : idx - n_own;
+                        const int per_blk = (kHalfTok - (o ? v_own : v_peer)) * 8;
+                        const int blk = x / per_blk, rem = x % per_blk;
+                        const int tok = (o ? v_own : v_peer) + rem / 8;
+                        const uint32_t slot = (o ? kSlotOwnV : 4 * peer) + blk;
+                        *reinterpret_cast<uint4 *>(stage + slot * kBox + tok * 128 + (rem % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + s));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ fix + epilogue warps
+        const int quarter = warp & 3;
+        const int h = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_off + kColO;
+        const float NEG_INF = -INFINITY;
+        uint32_t g = 0;
+        uint32_t n_cmd = 0;   // commands taken from the PV warp
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
             const int b = it.row / P.s_q;
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
-            const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
-
-            // q dims [128 half, 128 half + 128) of this head -> TMEM
-            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) break;
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    P.q_latent + ((size_t)it.row * kHeads + h) * kDl + 128 * half);
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t q[32];
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 x = src[c * 8 + v];
-                        q[4 * v] = x.x;
-                        q[4 * v + 1] = x.y;
-                        q[4 * v + 2] = x.z;
-                        q[4 * v + 3] = x.w;
-                    }
-                    tmem_st32(tQ + c * 32, q);
-                }
-                tmem_wait_st();
+            // q dims 192-383 of this head -> TMEM (for later items this happens
+            // before the previous item's epilogue, so that their scores overlap it)
+            if (ii == 0) {
+                load_q_part(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tmem + lane_off + kColQ, 1);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
@@ -450,127 +746,80 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
                 bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
             }
-            float m_run = NEG_INF, l_half = 0.f;
-            for (int k = 0; k < n; ++k, ++g) {
-                if (!wait_warp(ctl, bar(ctl, B_S_FULL), g & 1)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t r[32];
-                {   // this half's columns of both partial sums (dims 0-287, 288-575)
-                    uint32_t t[32];
-                    tmem_ld32(tS, r);
-                    tmem_ld32(tS + 64, t);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_S_EMPTY));
-
-                const int valid = (k == n - 1) ? valid_last : kPage;
-                uint8_t *stage = smem + kOffStage + (g % kStages) * kStageBytes;
-                float s[32];
-                float m_half = NEG_INF;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float a = __uint_as_float(r[j]) * P.scale_log2;
-                    a = 32 * half + j < valid ? a : NEG_INF;
-                    s[j] = a;
-                    m_half = fmaxf(m_half, a);
-                }
-                // row max over both halves (a block of this page the PV never reads)
-                float *pm = reinterpret_cast<float *>(stage + (rank == 0 ? 4 : 2) * kBlk);
-                pm[half * 128 + h] = m_half;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_PAIR + quarter));
-                if (!wait_warp(ctl, bar(ctl, B_PAIR + quarter), g & 1)) { ok = false; break; }
-                const float m_loc = fmaxf(m_half, pm[(1 - half) * 128 + h]);
-                // lazy rescale of the running output (the same decision in both halves)
-                float alpha = 1.f;
-                bool need = false;
-                if (k == 0) {
-                    m_run = m_loc;
-                } else if (m_loc > m_run + kRescaleThreshold) {
-                    alpha = fast_exp2(m_run - m_loc);
-                    m_run = m_loc;
-                    need = true;
-                }
-                // probabilities -> bf16 (registers)
-                uint32_t pk[16];
-                float lsum = 0.f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float e0 = fast_exp2(s[2 * j] - m_run);
-                    const float e1 = fast_exp2(s[2 * j + 1] - m_run);
-                    lsum += e0 + e1;
-                    pk[j] = pack_bf16(e0, e1);
-                }
-                // PV(g-1) must be done before O is rescaled
-                if (g >= 1 && !wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) { ok = false; break; }
+            // Fixes requested by the PV warp for pages of this item, then its end.
+            for (;;) {
+                if (!wait_warp(ctl, bar(ctl, B_CMD), n_cmd & 1)) { ok = false; break; }
+                ++n_cmd;
+                const int *cmd = reinterpret_cast<const int *>(smem + kOffRef + kRefCmd);
+                if (cmd[0] != 1) break;
+                const uint32_t s = (uint32_t)cmd[1];
+                const int k = cmd[2];
+                const uint32_t gp = (uint32_t)cmd[3];
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                const float o_ref = reinterpret_cast<const float *>(smem + kOffRef + kRefOld)[h];
+                const float m0 = *reinterpret_cast<const float *>(stage + kSlotRope * kBox + h * 8);
+                const float m1 = *reinterpret_cast<const float *>(stage + kSlotRope * kBox + 1024 + h * 8);
+                const float nref = fmaxf(o_ref, fmaxf(m0, m1));
+                // a half computed against a lower max is brought to the agreed one
+                uint8_t *prow = stage + 4 * rank * kBox + h * 128;
+                if (m0 != NEG_INF && m0 < nref) scale_p_half(prow, h, 0, fast_exp2(m0 - nref));
+                if (m1 != NEG_INF && m1 < nref) scale_p_half(prow, h, 1, fast_exp2(m1 - nref));
+                // O is rescaled once the previous PV is done
+                const bool need = k > 0 && nref > o_ref;
                 if (__any_sync(0xffffffffu, need)) {
+                    if (!wait_warp(ctl, bar(ctl, B_PVDONE + ((gp - 1) & 1)), ((gp - 1) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
+                    const float a = need ? fast_exp2(o_ref - nref) : 1.f;
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < 8; ++ch) {
                         uint32_t o[32];
                         tmem_ld32(tO + ch * 32, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
                         tmem_st32(tO + ch * 32, o);
                     }
                     tmem_wait_st();
                 }
-                l_half = l_half * alpha + lsum;
-                {   // this half's 32 tokens of the P row, K-major with the 128-byte swizzle
-                    uint8_t *prow = stage + (rank == 0 ? 7 : 0) * kBlk + h * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = 4 * half + cc;
-                        *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
-                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                    }
-                }
-                if (valid < kPage) {
-                    // zero this CTA's latent rows of the masked tail so that 0 * garbage stays 0
-                    uint8_t *vbase = stage + 4 * rank * kBlk;
-                    const int per_blk = (kPage - valid) * 8;  // 16-byte chunks per block
-                    for (int idx = sidx * 32 + lane; idx < 4 * per_blk; idx += 32 * kSoftmaxWarps) {
-                        const int blk = idx / per_blk, rem = idx % per_blk;
-                        const int tok = valid + rem / 8;
-                        *reinterpret_cast<uint4 *>(vbase + blk * kBlk + tok * 128 + (rem % 8) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_P_FULL));
+                if (lane == 0) mbar_arrive(bar(ctl, B_FIXED));
             }
+            g += n;
             if (!ok) break;
+            if (i + 1 < i_end) {
+                if (!wait_warp(ctl, bar(ctl, B_Q_EMPTY), ii & 1, kCluster)) break;
+                load_q_part(P.q_latent + ((size_t)items[i + 1].row * kHeads + h) * kDl,
+                            tmem + lane_off + kColQ, 1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
+            }
 
             // epilogue: wait for the last PV, normalise, store this CTA's half.  The
-            // rows go through the last page's stage (free now: its QK and PV are done
-            // and it is only refilled after this epilogue releases it) so that every
+            // rows go through the last page's stage (free now: its MMAs are done and
+            // it is only refilled after this epilogue releases it) so that every
             // global store writes 256 contiguous bytes of one row.
-            if (!wait_warp(ctl, bar(ctl, B_PV_DONE), (g - 1) & 1)) break;
+            // The item's last PV is done.  (The end command comes before that PV is
+            // issued, so the per-parity PV barriers may already be a phase further:
+            // a barrier with one phase per item keeps the wait exact.)
+            if (!wait_warp(ctl, bar(ctl, B_PVLAST), ii & 1)) break;
             tc_fence_after();
+            const float2 fin = reinterpret_cast<const float2 *>(smem + kOffRef + kRefFinal)[h];
+            const float l_run = fin.x, o_ref = fin.y;
             const uint32_t s_last = (g - 1) % kStages;
             uint8_t *lstage = smem + kOffStage + s_last * kStageBytes;
-            float *pl = reinterpret_cast<float *>(lstage + 8 * kBlk);  // row sums of both halves
-            pl[half * 128 + h] = l_half;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl, B_PAIRL + quarter));
-            if (!wait_warp(ctl, bar(ctl, B_PAIRL + quarter), ii & 1)) break;
-            const float l_run = pl[h] + pl[128 + h];   // the same order in both halves
             const float nan = __int_as_float(0x7fc00000);
             const float inv = bad ? nan : 1.f / l_run;
-            const float lse = bad ? nan : (m_run + log2f(l_run)) * 0.69314718055994531f;
-            uint8_t *stg = lstage + sidx * 8192;     // 32 rows x 256 B
+            const float lse = bad ? nan : (o_ref + log2f(l_run)) * 0.69314718055994531f;
+            uint8_t *stg = lstage + quarter * 8192;   // 32 rows x 256 B
             uint8_t *my_stg = stg + lane * 256;
             const bool final_out = it.part < 0;
-            const int passes = final_out ? 1 : 2;    // 256 B of a row per pass
+            const int passes = final_out ? 2 : 4;     // 256 B of a row per pass
 #pragma unroll 1
             for (int pass = 0; pass < passes; ++pass) {
                 // TMEM -> normalised values -> swizzled staging row (chunk c at c ^ lane)
@@ -578,7 +827,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 #pragma unroll 1
                     for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
-                        tmem_ld32(tO + ch * 32, o);
+                        tmem_ld32(tO + (pass * 4 + ch) * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -609,7 +858,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 if (pass == passes - 1) {  // O fully read: the next item's PV may overwrite it
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(ctl, B_O_FREE));
+                    if (lane == 0) mbar_arrive(bar(ctl, B_OFREE));
                 }
                 __syncwarp();
                 // staging -> global: two rows per step, 16 lanes x 16 B contiguous per row
@@ -620,28 +869,29 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 256 + ((j ^ (r & 15)) << 4));
                     const size_t hr = (size_t)it.row * kHeads + quarter * 32 + r;
                     if (final_out) {
-                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256 + half * 128)[j] = v;
+                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256 + pass * 128)[j] = v;
                     } else {
                         const size_t slot = (size_t)it.part * kHeads + quarter * 32 + r;
-                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + half * 128 +
-                                                  pass * 64)[j] = v;
+                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + pass * 64)[j] = v;
                     }
                 }
                 __syncwarp();
             }
-            if (rank == 0 && half == 0) {
+            if (rank == 0) {
                 if (final_out) P.lse[(size_t)it.row * kHeads + h] = lse;
                 else lse_part[(size_t)it.part * kHeads + h] = lse;
             }
-            if (bad && lane == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
-            // once every softmax warp is done with the stage, release it in both CTAs
+            if (bad && lane == 0 && rank == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
+            // once every merge warp is done with the stage, release it in both CTAs
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
-            if (warp == 2 && !wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
-            if (warp == 2 && lane == 0) {
-                mbar_arrive(bar(ctl, B_KV_EMPTY + s_last));
-                mbar_arrive_cluster(mapa(bar(ctl, B_KV_EMPTY + s_last), rank ^ 1u));
+            if (warp == kMergeWarp0) {
+                if (!wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
+                if (lane == 0) {
+                    mbar_arrive(bar(ctl, B_EMPTY_OWN + s_last));
+                    mbar_arrive_cluster(mapa(bar(ctl, B_EMPTY_PEER + s_last), peer));
+                }
             }
         }
     }
@@ -650,7 +900,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     tc_fence_before();
     __syncthreads();
     cluster_sync();
-    if (warp == 1) {
+    if (warp == kQkWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -759,7 +1009,7 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     {
         cuuint64_t dims[3] = {(cuuint64_t)kDrow, (cuuint64_t)kPage, (cuuint64_t)num_pages};
         cuuint64_t strides[2] = {(cuuint64_t)kDrow * 2, (cuuint64_t)kDrow * 2 * kPage};
-        cuuint32_t box[3] = {64, 64, 1};
+        cuuint32_t box[3] = {64, (cuuint32_t)kHalfTok, 1};
         if (!encode(&p.tm_kv, kv, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
