@@ -73,12 +73,8 @@ constexpr int kQTDims = 384;                      // q dims 0-383 live in TMEM
 constexpr uint32_t kQSBytes = 3 * kQBlk;          // q dims 384-575 in shared memory
 constexpr uint32_t kOffQS = 0;
 constexpr uint32_t kOffStage = kQSBytes;
-constexpr uint32_t kOffRef = kOffStage + kStages * kStageBytes;  // merge state, see kRef*
-constexpr uint32_t kRefMax = 0;       // agreed max per head after each page, 2 (page parity) x 128
-constexpr uint32_t kRefFinal = 1024;  // (row sum, max) per head at an item's end, 128 x float2
-constexpr uint32_t kRefOld = 2048;    // agreed max before a page that needs a fix, 128 floats
-constexpr uint32_t kRefCmd = 2560;    // command to the merge warps: type, stage, item page, page
-constexpr uint32_t kOffBar = kOffRef + 4096;
+constexpr uint32_t kOffRef = kOffStage + kStages * kStageBytes;  // agreed max, 2 x 128 floats
+constexpr uint32_t kOffBar = kOffRef + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers, + alignment slack
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -91,10 +87,10 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 //   slots 4(1-r)..   the peer's tokens, this CTA's output dims (PV operand)
 //   slots 8-11       own tokens, this CTA's output dims (score + PV operand)
 //   slot 12          own tokens, rope dims (score operand only), then the
-//                    two halves' (max, row sum) per head, 1 KB per CTA
+//                    two halves' (max, running row sum) per head, 1 KB per CTA
 constexpr uint32_t kSlotOwnV = 8;
 constexpr uint32_t kSlotRope = 12;
-constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, sum)
+constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, row sum)
 
 __host__ __device__ constexpr uint32_t own_slot(uint32_t rank, uint32_t blk) {
     return blk == 8 ? kSlotRope : (blk / 4 == rank ? kSlotOwnV + blk % 4 : 4 * rank + blk % 4);
@@ -123,14 +119,13 @@ enum : uint32_t {
     B_SEMPTY = B_QKP + 2,                // + page parity: scores read and the peer's seen, both CTAs
     B_SDONE = B_SEMPTY + 2,              // + stage: own P half written
     B_PMSG = B_SDONE + kStages,          // + stage: the peer's P half arrived (+tx)
-    B_RESDONE = B_PMSG + kStages,        // + page parity: agreed max published
+    B_PREADY = B_PMSG + kStages,         // + stage: P tile final, PV may run
+    B_RESDONE = B_PREADY + kStages,      // + page parity: agreed max published
     B_PVDONE = B_RESDONE + 2,            // + page parity: PV done
     B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
-    B_CMD = B_EPI + 1,                   // PV warp -> merge warps: a fix or an item's end
-    B_FIXED = B_CMD + 1,                 // merge warps -> PV warp: fix done
-    B_DRAIN = B_FIXED + 1,               // + issuer (0, 1: score, 2: PV)
+    B_DRAIN = B_EPI + 1,                 // + issuer (0, 1: score, 2: PV)
     B_COUNT = B_DRAIN + 3,
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
@@ -289,20 +284,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             mbar_init(bar(ctl, B_EMPTY_PEER + s), 1);
             mbar_init(bar(ctl, B_SDONE + s), 4);
             mbar_init(bar(ctl, B_PMSG + s), 128);
+            mbar_init(bar(ctl, B_PREADY + s), 4);
         }
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_SFULL + p), 1);
             mbar_init(bar(ctl, B_QKP + p), 1);
             mbar_init(bar(ctl, B_SEMPTY + p), 2 * 4);
-            mbar_init(bar(ctl, B_RESDONE + p), 1);
+            mbar_init(bar(ctl, B_RESDONE + p), 4);
         }
         mbar_init(bar(ctl, B_PVDONE), 1);
         mbar_init(bar(ctl, B_PVDONE + 1), 1);
         mbar_init(bar(ctl, B_PVLAST), 1);
         mbar_init(bar(ctl, B_OFREE), 4);
         mbar_init(bar(ctl, B_EPI), 4);
-        mbar_init(bar(ctl, B_CMD), 1);
-        mbar_init(bar(ctl, B_FIXED), 4);
         for (int d = 0; d < 3; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
         fence_mbar_init();
     }
@@ -436,8 +430,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
         constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
         const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
-        float m_ref[4], l_sum[4];   // PV warp: agreed max and row sum of heads 4 lane..+3
-        uint32_t n_fix = 0;
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -480,93 +472,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                     __syncwarp();
                 } else {
-                    // Merge the pair's halves of page g (each lane: heads 4 lane..+3),
-                    // then O_c (+)= [P_0 | P_1] . V_c.  Usually both halves used the
-                    // agreed max and nothing changes; otherwise the merge warps scale
-                    // the lower half's P rows (and O when the max grew) first.
-                    if (!wait_warp(ctl, bar(ctl, B_SDONE + s), (g / kStages) & 1) ||
-                        !wait_warp(ctl, bar(ctl, B_PMSG + s), (g / kStages) & 1, kCluster)) {
-                        ok = false;
-                        break;
-                    }
+                    // O_c (+)= [P_0 | P_1] . V_c once the merge warps released the P tile
+                    if (!wait_warp(ctl, bar(ctl, B_PREADY + s), (g / kStages) & 1)) { ok = false; break; }
                     if (k == 0 && ii > 0 && !wait_warp(ctl, bar(ctl, B_OFREE), (ii - 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    if (k == 0) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            m_ref[j] = -INFINITY;
-                            l_sum[j] = 0.f;
-                        }
-                    }
-                    const uint8_t *msg = smem + kOffStage + so + kSlotRope * kBox + lane * 32;
-                    float m0[4], m1[4], r0[4], r1[4], nref[4];
-                    {
-                        const float4 a0 = reinterpret_cast<const float4 *>(msg)[0];
-                        const float4 a1 = reinterpret_cast<const float4 *>(msg)[1];
-                        const float4 b0 = reinterpret_cast<const float4 *>(msg + 1024)[0];
-                        const float4 b1 = reinterpret_cast<const float4 *>(msg + 1024)[1];
-                        m0[0] = a0.x; r0[0] = a0.y; m0[1] = a0.z; r0[1] = a0.w;
-                        m0[2] = a1.x; r0[2] = a1.y; m0[3] = a1.z; r0[3] = a1.w;
-                        m1[0] = b0.x; r1[0] = b0.y; m1[1] = b0.z; r1[1] = b0.w;
-                        m1[2] = b1.x; r1[2] = b1.y; m1[3] = b1.z; r1[3] = b1.w;
-                    }
-                    bool fix = false;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        nref[j] = fmaxf(m_ref[j], fmaxf(m0[j], m1[j]));   // finite: token 0 is valid
-                        fix |= (m0[j] != -INFINITY && m0[j] < nref[j]) ||
-                               (m1[j] != -INFINITY && m1[j] < nref[j]) || (k > 0 && nref[j] > m_ref[j]);
-                    }
-                    if (__any_sync(0xffffffffu, fix)) {
-                        // hand the page to the merge warps (they recompute the same factors)
-                        float *old = reinterpret_cast<float *>(smem + kOffRef + kRefOld);
-                        reinterpret_cast<float4 *>(old)[lane] = make_float4(m_ref[0], m_ref[1], m_ref[2], m_ref[3]);
-                        __threadfence_block();
-                        if (lane == 0) {
-                            int *cmd = reinterpret_cast<int *>(smem + kOffRef + kRefCmd);
-                            cmd[0] = 1;
-                            cmd[1] = (int)s;
-                            cmd[2] = k;
-                            cmd[3] = (int)g;
-                        }
-                        __syncwarp();
-                        if (elect_one()) mbar_arrive(bar(ctl, B_CMD));
-                        if (!wait_warp(ctl, bar(ctl, B_FIXED), n_fix & 1)) { ok = false; break; }
-                        ++n_fix;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float f0 = m0[j] == -INFINITY ? 0.f : (m0[j] == nref[j] ? 1.f : fast_exp2(m0[j] - nref[j]));
-                        const float f1 = m1[j] == -INFINITY ? 0.f : (m1[j] == nref[j] ? 1.f : fast_exp2(m1[j] - nref[j]));
-                        const float alpha = m_ref[j] == -INFINITY ? 0.f
-                                            : (nref[j] > m_ref[j] ? fast_exp2(m_ref[j] - nref[j]) : 1.f);
-                        l_sum[j] = l_sum[j] * alpha + r0[j] * f0 + r1[j] * f1;   // same order in both CTAs
-                        m_ref[j] = nref[j];
-                    }
-                    // the agreed max after page g, for the softmax of page g + 2
-                    float *mref = reinterpret_cast<float *>(smem + kOffRef + kRefMax);
-                    reinterpret_cast<float4 *>(mref + (g & 1) * 128)[lane] =
-                        make_float4(m_ref[0], m_ref[1], m_ref[2], m_ref[3]);
-                    if (k == n - 1) {
-                        float4 *fin = reinterpret_cast<float4 *>(smem + kOffRef + kRefFinal);
-                        fin[2 * lane] = make_float4(l_sum[0], m_ref[0], l_sum[1], m_ref[1]);
-                        fin[2 * lane + 1] = make_float4(l_sum[2], m_ref[2], l_sum[3], m_ref[3]);
-                    }
-                    __threadfence_block();
-                    __syncwarp();
-                    if (elect_one()) {
-                        mbar_arrive(bar(ctl, B_RESDONE + (g & 1)));
-                        if (k == n - 1) {   // the item's end: the merge warps run the epilogue
-                            int *cmd = reinterpret_cast<int *>(smem + kOffRef + kRefCmd);
-                            cmd[0] = 2;
-                            mbar_arrive(bar(ctl, B_CMD));
-                        }
-                    }
-                    // P halves (generic stores here and st.async from the peer) -> tensor cores
-                    fence_proxy_async_smem();
-                    __syncwarp();
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
@@ -628,6 +539,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
             float m_prev = NEG_INF;   // max used for this half's previous page
+            float l_own = 0.f;        // row sum of this half's tokens so far, relative to m_prev
             for (int k = 0; k < n; ++k, ++g) {
                 const uint32_t par = g & 1, s = g % kStages;
                 // Start from the pair's agreed max of two pages back (a fixed point
@@ -656,6 +568,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 }
                 // raise the max only when this half's page exceeds it by > 2^8
                 const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
+                const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : fast_exp2(m_prev - m_used));
                 m_prev = m_used;
                 const float mu = m_used == NEG_INF ? 0.f : m_used;
                 uint32_t pk[16];
@@ -667,6 +580,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     rsum += e0 + e1;
                     pk[j] = pack_bf16(e0, e1);
                 }
+                l_own = l_own * l_scale + rsum;
                 // P half -> this CTA's P tile and the peer's (once the peer's scores,
                 // which read those slots, are done), with (max, row sum)
                 if (!wait_warp(ctl, bar(ctl, B_QKP + par), (g >> 1) & 1, kSignal)) { ok = false; break; }
@@ -692,8 +606,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 }
                 {
                     const uint32_t off = kSlotRope * kBox + rank * 1024 + h * 8;
-                    *reinterpret_cast<float2 *>(stage + off) = make_float2(m_used, rsum);
-                    st_async_v2_f32(mapa(s_stg + off, peer), m_used, rsum, pmsg_peer);
+                    *reinterpret_cast<float2 *>(stage + off) = make_float2(m_used, l_own);
+                    st_async_v2_f32(mapa(s_stg + off, peer), m_used, l_own, pmsg_peer);
                 }
                 if (valid < kPage) {
                     // zero this CTA's latent rows of the masked tail (own and peer tokens)
@@ -717,14 +631,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
         }
     } else {
-        // ------------------------------------------------------------ fix + epilogue warps
+        // ------------------------------------------------------------ merge + epilogue warps
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_off + kColO;
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
-        uint32_t n_cmd = 0;   // commands taken from the PV warp
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
@@ -746,33 +659,35 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
                 bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
             }
-            // Fixes requested by the PV warp for pages of this item, then its end.
-            for (;;) {
-                if (!wait_warp(ctl, bar(ctl, B_CMD), n_cmd & 1)) { ok = false; break; }
-                ++n_cmd;
-                const int *cmd = reinterpret_cast<const int *>(smem + kOffRef + kRefCmd);
-                if (cmd[0] != 1) break;
-                const uint32_t s = (uint32_t)cmd[1];
-                const int k = cmd[2];
-                const uint32_t gp = (uint32_t)cmd[3];
+            // Merge the pair's halves of each page: agree on the max per head (a
+            // half computed against a lower one is scaled; O is rescaled when the
+            // agreed max grows), publish it for the softmax two pages on and
+            // release the P tile to the PV warp.  Each half's message carries its
+            // running row sum, so the sums are combined once, at the last page.
+            float m_ref = NEG_INF, l_run = 0.f;
+            for (int k = 0; k < n; ++k) {
+                const uint32_t gp = g + k, par = gp & 1, s = gp % kStages;
+                if (!wait_warp(ctl, bar(ctl, B_SDONE + s), (gp / kStages) & 1) ||
+                    !wait_warp(ctl, bar(ctl, B_PMSG + s), (gp / kStages) & 1, kCluster)) {
+                    ok = false;
+                    break;
+                }
                 uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                const float o_ref = reinterpret_cast<const float *>(smem + kOffRef + kRefOld)[h];
-                const float m0 = *reinterpret_cast<const float *>(stage + kSlotRope * kBox + h * 8);
-                const float m1 = *reinterpret_cast<const float *>(stage + kSlotRope * kBox + 1024 + h * 8);
-                const float nref = fmaxf(o_ref, fmaxf(m0, m1));
-                // a half computed against a lower max is brought to the agreed one
+                const float2 h0 = *reinterpret_cast<const float2 *>(stage + kSlotRope * kBox + h * 8);
+                const float2 h1 = *reinterpret_cast<const float2 *>(stage + kSlotRope * kBox + 1024 + h * 8);
+                const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
                 uint8_t *prow = stage + 4 * rank * kBox + h * 128;
-                if (m0 != NEG_INF && m0 < nref) scale_p_half(prow, h, 0, fast_exp2(m0 - nref));
-                if (m1 != NEG_INF && m1 < nref) scale_p_half(prow, h, 1, fast_exp2(m1 - nref));
-                // O is rescaled once the previous PV is done
-                const bool need = k > 0 && nref > o_ref;
+                if (h0.x != NEG_INF && h0.x < nref) scale_p_half(prow, h, 0, fast_exp2(h0.x - nref));
+                if (h1.x != NEG_INF && h1.x < nref) scale_p_half(prow, h, 1, fast_exp2(h1.x - nref));
+                // O is rescaled (rarely) once the previous PV is done
+                const bool need = k > 0 && nref > m_ref;
                 if (__any_sync(0xffffffffu, need)) {
-                    if (!wait_warp(ctl, bar(ctl, B_PVDONE + ((gp - 1) & 1)), ((gp - 1) >> 1) & 1)) {
+                    if (!wait_warp(ctl, bar(ctl, B_PVDONE + (par ^ 1)), ((gp - 1) >> 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const float a = need ? fast_exp2(o_ref - nref) : 1.f;
+                    const float a = need ? fast_exp2(m_ref - nref) : 1.f;
 #pragma unroll 1
                     for (int ch = 0; ch < 8; ++ch) {
                         uint32_t o[32];
@@ -784,10 +699,20 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                     tmem_wait_st();
                 }
+                m_ref = nref;
+                oref[par * 128 + h] = m_ref;
+                if (k == n - 1) {   // both halves' row sums, relative to the final max (same order in both CTAs)
+                    const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : fast_exp2(h0.x - nref));
+                    const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : fast_exp2(h1.x - nref));
+                    l_run = h0.y * f0 + h1.y * f1;
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_FIXED));
+                if (lane == 0) {
+                    mbar_arrive(bar(ctl, B_RESDONE + par));
+                    mbar_arrive(bar(ctl, B_PREADY + s));
+                }
             }
             g += n;
             if (!ok) break;
@@ -809,8 +734,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             // a barrier with one phase per item keeps the wait exact.)
             if (!wait_warp(ctl, bar(ctl, B_PVLAST), ii & 1)) break;
             tc_fence_after();
-            const float2 fin = reinterpret_cast<const float2 *>(smem + kOffRef + kRefFinal)[h];
-            const float l_run = fin.x, o_ref = fin.y;
+            const float o_ref = m_ref;
             const uint32_t s_last = (g - 1) % kStages;
             uint8_t *lstage = smem + kOffStage + s_last * kStageBytes;
             const float nan = __int_as_float(0x7fc00000);
