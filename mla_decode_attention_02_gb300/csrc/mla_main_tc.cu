@@ -13,34 +13,38 @@
 // two CTAs on two SMs: CTA c owns output columns [256c, 256c + 256) and the
 // tokens [32c, 32c + 32) of every 64-token page.
 //
-//   page g -> TMA: each CTA loads its own 32 tokens (all 576 dims); the
-//             dims the peer's PV needs go to both CTAs (multicast)
 //   S_c = q . k_c^T     tcgen05 M=128 (heads) N=32 (own tokens) K=576, fp32
 //                       in TMEM; q dims 0-383 are the A operand in TMEM,
 //                       384-575 in shared memory
 //   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, written into
 //                       this CTA's P tile and the peer's (st.async, 8 KB)
 //   merge: the pair agrees on the running max per head (each side's max
-//          travels with its P half; the lower half is scaled), keeps the
-//          row sum of both halves and rescales O when the max grows
+//          travels with its P half; the lower half is scaled) and rescales
+//          O when the max grows; each half's running row sum rides along
 //   O_c += [P_0 | P_1] . V_c   tcgen05 M=128 N=256 K=64, V_c = the page's
 //                       latent dims [256c, 256c + 256) of all 64 tokens
 //
-// Measured on this part: one SM's shared memory streams about 250 GB/s,
-// and each page costs this layout ~200 KB of shared-memory traffic per SM
-// (ingest 52 KB, score operands 84 KB, PV operands 48 KB, P 16 KB) against
-// ~290 KB when each CTA scores the whole page; distributed shared memory
-// moves only 15-20 GB/s per SM, which the 8 KB P half per page fits.
+// Two page rings.  The K ring holds this CTA's 32 tokens of a page (all 576
+// dims, 36 KB) and is released as soon as the score MMAs are done; the V
+// ring holds the page's 64 tokens of this CTA's 256 output dims (32 KB, own
+// tokens loaded a second time, from L2), the P tile and the two halves'
+// messages, and is released by PV.  The score chain (load -> MMA) thus never
+// waits for the softmax, the exchange or PV of earlier pages.
+//
+// Measured on this part: one SM's shared memory streams about 250 GB/s, and
+// scoring only the own half keeps the traffic near 220 KB per page and SM;
+// distributed shared memory moves only 15-20 GB/s per SM, which the 8 KB P
+// half per page fits.
 //
 // TMEM (512 columns): O half [0,256), S (two pages) [256,320), q [320,512).
-// Warp roles per CTA: warp 0 issues TMA; warps 1 and 2 issue the score
-// products of even and odd pages and warp 3 the PV product (each a whole
-// warp that waits together and issues from one elected lane: about 15 ns per
-// tcgen05.mma, against 35 ns from a lane-0 branch); warps 4-7 (one per TMEM
-// lane quarter, one thread per head) load q into TMEM and compute P; warps
-// 8-11 merge the two halves and run the epilogue.  Every wait is bounded: on
-// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
-// hanging.
+// Warp roles per CTA: warp 0 loads the K ring and q; warps 1 and 2 issue
+// the score products of even and odd pages and warp 3 the PV product (each a
+// whole warp that waits together and issues from one elected lane: about
+// 15 ns per tcgen05.mma, against 35 ns from a lane-0 branch); warps 4-7 (one
+// per TMEM lane quarter, one thread per head) load q into TMEM and compute P;
+// warps 8-11 merge the two halves and run the epilogue, and warp 8 loads the
+// V ring (page g + 1 as soon as page g is merged).  Every wait is bounded: on time-out the kernel records
+// MLA_DEV_TIMEOUT and winds down instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -61,40 +65,31 @@ constexpr int kQkWarp0 = 1;         // warps 1, 2: score MMAs of even, odd pages
 constexpr int kPvWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;    // warps 4-7
 constexpr int kMergeWarp0 = 8;      // warps 8-11
-constexpr int kStages = 3;          // KV page ring
+constexpr int kKStages = 2;         // K ring (indexed by page parity)
+constexpr int kVStages = 2;         // V ring (indexed by page parity)
 constexpr int kPrefetch = 3;        // L2 prefetch distance in pages
 constexpr int kClusterSize = 2;
 constexpr uint16_t kBoth = 0x3;
 constexpr int kHalfTok = 32;                      // tokens of a page per CTA
 constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-byte swizzle
-constexpr uint32_t kStageBytes = 13 * kBox;       // 13 boxes land in each CTA per page
+constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
 constexpr int kQTDims = 384;                      // q dims 0-383 live in TMEM
 constexpr uint32_t kQSBytes = 3 * kQBlk;          // q dims 384-575 in shared memory
+// V stage: own tokens' output dims, peer tokens' output dims, P tile, messages
+constexpr uint32_t kVOwn = 0, kVPeer = 4 * kBox, kVP = 8 * kBox, kVMsg = 12 * kBox;
+constexpr uint32_t kVStageBytes = kVMsg + 2048;
 constexpr uint32_t kOffQS = 0;
-constexpr uint32_t kOffStage = kQSBytes;
-constexpr uint32_t kOffRef = kOffStage + kStages * kStageBytes;  // agreed max, 2 x 128 floats
+constexpr uint32_t kOffK = kQSBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kKStageBytes;
+constexpr uint32_t kOffRef = kOffV + kVStages * kVStageBytes;  // agreed max, 2 x 128 floats
 constexpr uint32_t kOffBar = kOffRef + 1024;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers, + alignment slack
-static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "TMA/UMMA tile alignment");
+static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kOffV % 1024 == 0 &&
+                  kVStageBytes % 1024 == 0,
+              "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-// Stage layout (4 KB slots).  Rank r loads its own token half (tokens 32r..)
-// of all nine 64-dim blocks; the four blocks holding the peer's output dims
-// are multicast, so both CTAs see them at the same offset.
-//   slots 4r..4r+3   own tokens, the peer's output dims: score operand only,
-//                    then this CTA's P tile (128 heads x 64 tokens, bf16)
-//   slots 4(1-r)..   the peer's tokens, this CTA's output dims (PV operand)
-//   slots 8-11       own tokens, this CTA's output dims (score + PV operand)
-//   slot 12          own tokens, rope dims (score operand only), then the
-//                    two halves' (max, running row sum) per head, 1 KB per CTA
-constexpr uint32_t kSlotOwnV = 8;
-constexpr uint32_t kSlotRope = 12;
 constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, row sum)
-
-__host__ __device__ constexpr uint32_t own_slot(uint32_t rank, uint32_t blk) {
-    return blk == 8 ? kSlotRope : (blk / 4 == rank ? kSlotOwnV + blk % 4 : 4 * rank + blk % 4);
-}
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
@@ -106,22 +101,24 @@ static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: raise the max only when it grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
-// barrier slots (8 bytes each) in the barrier area
+// barrier slots (8 bytes each) in the barrier area; "+ p" = page parity
 enum : uint32_t {
     B_Q_FULL = 0,                        // producer (+tx), softmax and merge warps (q in TMEM)
     B_Q_EMPTY = 1,                       // both score issuers of both CTAs done with q
-    B_FULL = 2,                          // + stage: dim blocks 0-5 of the page landed (+tx)
-    B_FULLB = B_FULL + kStages,          // + stage: the rest landed (+tx)
-    B_EMPTY_OWN = B_FULLB + kStages,     // + stage: this CTA's PV done with the stage
-    B_EMPTY_PEER = B_EMPTY_OWN + kStages,  // + stage: the peer's PV done with its copy
-    B_SFULL = B_EMPTY_PEER + kStages,    // + page parity: scores in TMEM
-    B_QKP = B_SFULL + 2,                 // + page parity: the peer's scores done
-    B_SEMPTY = B_QKP + 2,                // + page parity: scores read and the peer's seen, both CTAs
-    B_SDONE = B_SEMPTY + 2,              // + stage: own P half written
-    B_PMSG = B_SDONE + kStages,          // + stage: the peer's P half arrived (+tx)
-    B_PREADY = B_PMSG + kStages,         // + stage: P tile final, PV may run
-    B_RESDONE = B_PREADY + kStages,      // + page parity: agreed max published
-    B_PVDONE = B_RESDONE + 2,            // + page parity: PV done
+    B_KFULL = 2,                         // + p: dim blocks 0-5 of the K stage landed (+tx)
+    B_KFULLB = B_KFULL + 2,              // + p: blocks 6-8 landed (+tx)
+    B_KEMPTY = B_KFULLB + 2,             // + p: score MMAs done with the K stage
+    B_VFULL = B_KEMPTY + 2,              // + p: V stage landed (+tx)
+    B_VEMPTY = B_VFULL + 2,              // + p: this CTA's PV done with the V stage
+    B_VEMPTY_PEER = B_VEMPTY + 2,        // + p: the peer's PV done with its V stage
+    B_SFULL = B_VEMPTY_PEER + 2,         // + p: scores in TMEM
+    B_QKP = B_SFULL + 2,                 // + p: the peer's scores done
+    B_SEMPTY = B_QKP + 2,                // + p: scores read and the peer's seen, both CTAs
+    B_SDONE = B_SEMPTY + 2,              // + p: own P half written
+    B_PMSG = B_SDONE + 2,                // + p: the peer's P half arrived (+tx)
+    B_PREADY = B_PMSG + 2,               // + p: P tile final, PV may run
+    B_RESDONE = B_PREADY + 2,            // + p: agreed max published
+    B_PVDONE = B_RESDONE + 2,            // + p: PV done
     B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
@@ -256,7 +253,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t s_base = smem_u32(smem);
     const uint32_t s_qs = s_base + kOffQS;
-    const uint32_t s_stage = s_base + kOffStage;
+    const uint32_t s_k = s_base + kOffK;
+    const uint32_t s_v = s_base + kOffV;
     float *oref = reinterpret_cast<float *>(smem + kOffRef);  // [page parity][head]
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -277,23 +275,22 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         abort_flag = 0;
         mbar_init(bar(ctl, B_Q_FULL), 1 + 8);
         mbar_init(bar(ctl, B_Q_EMPTY), 2 * kClusterSize);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(ctl, B_FULL + s), 1);
-            mbar_init(bar(ctl, B_FULLB + s), 1);
-            mbar_init(bar(ctl, B_EMPTY_OWN + s), 1);
-            mbar_init(bar(ctl, B_EMPTY_PEER + s), 1);
-            mbar_init(bar(ctl, B_SDONE + s), 4);
-            mbar_init(bar(ctl, B_PMSG + s), 128);
-            mbar_init(bar(ctl, B_PREADY + s), 4);
-        }
         for (int p = 0; p < 2; ++p) {
+            mbar_init(bar(ctl, B_KFULL + p), 1);
+            mbar_init(bar(ctl, B_KFULLB + p), 1);
+            mbar_init(bar(ctl, B_KEMPTY + p), 1);
+            mbar_init(bar(ctl, B_VFULL + p), 1);
+            mbar_init(bar(ctl, B_VEMPTY + p), 1);
+            mbar_init(bar(ctl, B_VEMPTY_PEER + p), 1);
             mbar_init(bar(ctl, B_SFULL + p), 1);
             mbar_init(bar(ctl, B_QKP + p), 1);
             mbar_init(bar(ctl, B_SEMPTY + p), 2 * 4);
+            mbar_init(bar(ctl, B_SDONE + p), 4);
+            mbar_init(bar(ctl, B_PMSG + p), 128);
+            mbar_init(bar(ctl, B_PREADY + p), 4);
             mbar_init(bar(ctl, B_RESDONE + p), 4);
+            mbar_init(bar(ctl, B_PVDONE + p), 1);
         }
-        mbar_init(bar(ctl, B_PVDONE), 1);
-        mbar_init(bar(ctl, B_PVDONE + 1), 1);
         mbar_init(bar(ctl, B_PVLAST), 1);
         mbar_init(bar(ctl, B_OFREE), 4);
         mbar_init(bar(ctl, B_EPI), 4);
@@ -334,9 +331,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     } else if (threadIdx.x == 0 && rank == 0) {
         atomicOr(&hdr->status, MLA_DEV_BAD_PLAN);
     }
+    const int tok_own = kHalfTok * (int)rank, tok_peer = kHalfTok * (int)peer;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ K ring producer
+        // This CTA's tokens of each page (all dims) and q.  Out-of-pool page
+        // indices read zeros (TMA bounds fill); the merge warps flag the row.
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -346,7 +346,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
             const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
-            const int tok0 = kHalfTok * (int)rank;
             for (int k0 = 0; k0 < n && ok; k0 += 32) {
                 const int mine = k0 + lane < n ? bt[k0 + lane] : 0;
                 const int ahead = k0 + lane + kPrefetch < n ? bt[k0 + lane + kPrefetch] : 0;
@@ -354,38 +353,22 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 for (int kk = 0; kk < cnt; ++kk, ++g) {
                     const int page = __shfl_sync(0xffffffffu, mine, kk);
                     const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
-                    const uint32_t s = g % kStages;
-                    // our loads write into both CTAs: both copies of the stage must be free
-                    if (g >= kStages) {
-                        const uint32_t par = ((g / kStages) - 1) & 1;
-                        if (!wait_warp(ctl, bar(ctl, B_EMPTY_OWN + s), par) ||
-                            !wait_warp(ctl, bar(ctl, B_EMPTY_PEER + s), par, kSignal)) {
-                            ok = false;
-                            break;
-                        }
+                    const uint32_t p = g & 1;
+                    if (g >= 2 && !wait_warp(ctl, bar(ctl, B_KEMPTY + p), ((g >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
                     if (lane == 0) {
-                        // Blocks 0-5 (the score MMAs with q in TMEM) and 6-8 complete
-                        // separate barriers, so that those MMAs start before the rest
-                        // lands.  A multicast block completes the same barrier in both
-                        // CTAs: group A here also receives the peer's blocks 4r..4r+3
-                        // that lie below 6.
-                        const uint32_t fa = bar(ctl, B_FULL + s), fb = bar(ctl, B_FULLB + s);
-                        const uint32_t dst = s_stage + s * kStageBytes;
-                        const uint32_t bytes_a = (6 + (rank == 0 ? 4 : 2)) * kBox;
-                        mbar_arrive_expect_tx(fa, bytes_a);
-                        mbar_arrive_expect_tx(fb, kStageBytes - bytes_a);
-                        // An out-of-pool page index reads zeros (TMA bounds fill);
-                        // the merge warps flag the row.
+                        // blocks 0-5 (score MMAs with q in TMEM) and 6-8 complete
+                        // separate barriers, so those MMAs start before the rest lands
+                        const uint32_t fa = bar(ctl, B_KFULL + p), fb = bar(ctl, B_KFULLB + p);
+                        const uint32_t dst = s_k + p * kKStageBytes;
+                        mbar_arrive_expect_tx(fa, 6 * kBox);
+                        mbar_arrive_expect_tx(fb, 3 * kBox);
 #pragma unroll
-                        for (uint32_t blk = 0; blk < 9; ++blk) {
-                            const uint32_t d = dst + own_slot(rank, blk) * kBox;
-                            const uint32_t fbar = blk < 6 ? fa : fb;
-                            if (blk < 8 && blk / 4 != rank)
-                                tma_load_3d_mc(d, &P.tm_kv, 64 * blk, tok0, page, fbar, kBoth);
-                            else
-                                tma_load_3d(d, &P.tm_kv, 64 * blk, tok0, page, fbar);
-                        }
+                        for (int blk = 0; blk < 9; ++blk)
+                            tma_load_3d(dst + blk * kBox, &P.tm_kv, 64 * blk, tok_own, page,
+                                        blk < 6 ? fa : fb);
                     }
                     if (k0 + kk == 0) {
                         // q dims 384-575, once the first page is on its way: both CTAs'
@@ -406,10 +389,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             }
                         }
                     }
-                    // warm L2 for a page beyond the stages in flight
+                    // warm L2 for a page beyond the ones in flight (each CTA warms its
+                    // own token half, which the peer's V ring reads as well)
                     if (lane == 0 && k0 + kk + kPrefetch < n)
                         for (int blk = 0; blk < 9; ++blk)
-                            tma_prefetch_3d(&P.tm_kv, 64 * blk, tok0, page_ahead);
+                            tma_prefetch_3d(&P.tm_kv, 64 * blk, tok_own, page_ahead);
                     __syncwarp();
                 }
             }
@@ -418,15 +402,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         // ------------------------------------------------------------ MMA issuers
         // The whole warp runs the schedule and waits; one elected lane issues.
         const int role = warp - kQkWarp0;   // 0, 1: score MMAs of even / odd pages; 2: PV
-        uint32_t slot_off[9];
-#pragma unroll
-        for (uint32_t blk = 0; blk < 9; ++blk) slot_off[blk] = own_slot(rank, blk) * kBox;
         // Descriptor bases; every MMA below adds a byte offset (>> 4).
         const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
-        const uint64_t d_st = smem_desc(s_stage, 16, 1024, 2);
-        const uint64_t d_p = smem_desc(s_stage + 4 * rank * kBox, 16, 1024, 2);
-        const uint64_t d_vown = smem_desc(s_stage + kSlotOwnV * kBox, 4096, 1024, 2);
-        const uint64_t d_vpeer = smem_desc(s_stage + 4 * peer * kBox, 4096, 1024, 2);
+        const uint64_t d_k = smem_desc(s_k, 16, 1024, 2);
+        const uint64_t d_p = smem_desc(s_v + kVP, 16, 1024, 2);
+        const uint64_t d_vown = smem_desc(s_v + kVOwn, 4096, 1024, 2);
+        const uint64_t d_vpeer = smem_desc(s_v + kVPeer, 4096, 1024, 2);
         constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
         constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
         const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
@@ -439,41 +420,48 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             // every score issuer takes part in every item's q hand-over, pages or not
             if (role < 2 && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
             for (int k = 0; k < n && ok; ++k, ++g) {
-                const uint32_t s = g % kStages;
-                const uint32_t so = s * kStageBytes;
+                const uint32_t p = g & 1;
                 if (role < 2) {
-                    if ((int)(g & 1) != role) continue;
-                    if (!wait_warp(ctl, bar(ctl, B_FULL + s), (g / kStages) & 1)) { ok = false; break; }
+                    if ((int)p != role) continue;
+                    const uint32_t ko = p * kKStageBytes;
+                    if (!wait_warp(ctl, bar(ctl, B_KFULL + p), (g >> 1) & 1)) { ok = false; break; }
                     if (g >= 2 &&
-                        !wait_warp(ctl, bar(ctl, B_SEMPTY + role), ((g >> 1) - 1) & 1, kSignal)) {
+                        !wait_warp(ctl, bar(ctl, B_SEMPTY + p), ((g >> 1) - 1) & 1, kSignal)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t tS = tmem + kColS + kHalfTok * role;
+                    const uint32_t tS = tmem + kColS + kHalfTok * p;
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 0; ks < 24; ++ks)
                             mma_ts(tS, tQ + 8 * ks,
-                                   d_st + (uint64_t)((so + slot_off[ks >> 2] + (ks & 3) * 32) >> 4),
+                                   d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, ks > 0 ? 1u : 0u);
                     }
                     __syncwarp();
-                    if (!wait_warp(ctl, bar(ctl, B_FULLB + s), (g / kStages) & 1)) { ok = false; break; }
+                    if (!wait_warp(ctl, bar(ctl, B_KFULLB + p), (g >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 24; ks < 36; ++ks)
                             mma_ss(tS, d_qs + (uint64_t)((((ks - 24) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
-                                   d_st + (uint64_t)((so + slot_off[ks >> 2] + (ks & 3) * 32) >> 4),
+                                   d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, 1u);
-                        mma_commit(bar(ctl, B_SFULL + role));
-                        mma_commit_mc(bar(ctl, B_QKP + role), peer_mask);
+                        mma_commit(bar(ctl, B_SFULL + p));
+                        mma_commit_mc(bar(ctl, B_QKP + p), peer_mask);
+                        mma_commit(bar(ctl, B_KEMPTY + p));
                     }
                     __syncwarp();
                 } else {
-                    // O_c (+)= [P_0 | P_1] . V_c once the merge warps released the P tile
-                    if (!wait_warp(ctl, bar(ctl, B_PREADY + s), (g / kStages) & 1)) { ok = false; break; }
+                    // O_c (+)= [P_0 | P_1] . V_c once the V stage landed and the merge
+                    // warps released the P tile
+                    const uint32_t vo = p * kVStageBytes;
+                    if (!wait_warp(ctl, bar(ctl, B_VFULL + p), (g >> 1) & 1) ||
+                        !wait_warp(ctl, bar(ctl, B_PREADY + p), (g >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
                     if (k == 0 && ii > 0 && !wait_warp(ctl, bar(ctl, B_OFREE), (ii - 1) & 1)) {
                         ok = false;
                         break;
@@ -483,16 +471,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint64_t vb = (uint32_t)(ks >> 1) == rank ? d_vown : d_vpeer;
-                            mma_ss(tO, d_p + (uint64_t)((so + ks * 32) >> 4),
-                                   vb + (uint64_t)((so + (ks & 1) * 2048) >> 4), id_pv,
+                            mma_ss(tO, d_p + (uint64_t)((vo + ks * 32) >> 4),
+                                   vb + (uint64_t)((vo + (ks & 1) * 2048) >> 4), id_pv,
                                    (k == 0 && ks == 0) ? 0u : 1u);
                         }
-                        mma_commit(bar(ctl, B_PVDONE + (g & 1)));
-                        // the last page's stage is released by the epilogue, which
+                        mma_commit(bar(ctl, B_PVDONE + p));
+                        // the last page's V stage is released by the epilogue, which
                         // stages the output through it
                         if (k != n - 1) {
-                            mma_commit(bar(ctl, B_EMPTY_OWN + s));
-                            mma_commit_mc(bar(ctl, B_EMPTY_PEER + s), peer_mask);
+                            mma_commit(bar(ctl, B_VEMPTY + p));
+                            mma_commit_mc(bar(ctl, B_VEMPTY_PEER + p), peer_mask);
                         } else {
                             mma_commit(bar(ctl, B_PVLAST));
                         }
@@ -541,7 +529,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             float m_prev = NEG_INF;   // max used for this half's previous page
             float l_own = 0.f;        // row sum of this half's tokens so far, relative to m_prev
             for (int k = 0; k < n; ++k, ++g) {
-                const uint32_t par = g & 1, s = g % kStages;
+                const uint32_t par = g & 1;
                 // Start from the pair's agreed max of two pages back (a fixed point
                 // in the schedule, so the result does not depend on timing).  The
                 // wait is taken on every page so that no phase of the barrier is
@@ -558,14 +546,23 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 tmem_wait_ld();
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
-                const int v_own = min(max(valid - kHalfTok * (int)rank, 0), kHalfTok);
-                float lm = NEG_INF;
+                const int v_own = min(max(valid - tok_own, 0), kHalfTok);
+                // scores in log2 units are r * scale_log2 (scale > 0, so the max of
+                // the raw scores gives the max); masked tokens (ragged last page)
+                // are -inf
+                const float sc = P.scale_log2;
+                float rmax = -INFINITY;
+                if (v_own == kHalfTok) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float a = j < v_own ? __uint_as_float(r[j]) * P.scale_log2 : NEG_INF;
-                    r[j] = __float_as_uint(a);
-                    lm = fmaxf(lm, a);
+                    for (int j = 0; j < 32; ++j) rmax = fmaxf(rmax, __uint_as_float(r[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j >= v_own) r[j] = __float_as_uint(NEG_INF);
+                        rmax = fmaxf(rmax, __uint_as_float(r[j]));
+                    }
                 }
+                const float lm = rmax * sc;
                 // raise the max only when this half's page exceeds it by > 2^8
                 const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
                 const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : fast_exp2(m_prev - m_used));
@@ -575,59 +572,55 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 float rsum = 0.f;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float e0 = fast_exp2(__uint_as_float(r[2 * j]) - mu);
-                    const float e1 = fast_exp2(__uint_as_float(r[2 * j + 1]) - mu);
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(r[2 * j]), sc, -mu));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(r[2 * j + 1]), sc, -mu));
                     rsum += e0 + e1;
                     pk[j] = pack_bf16(e0, e1);
                 }
                 l_own = l_own * l_scale + rsum;
-                // P half -> this CTA's P tile and the peer's (once the peer's scores,
-                // which read those slots, are done), with (max, row sum)
+                // The score buffer is released in both CTAs once the peer's scores of
+                // this page are seen: the peer's scores of page g + 2 (which complete
+                // the next phase of this parity's QKP barrier) wait for it, so no
+                // phase is skipped.
                 if (!wait_warp(ctl, bar(ctl, B_QKP + par), (g >> 1) & 1, kSignal)) { ok = false; break; }
-                // The score buffer is released in both CTAs only now: the peer's
-                // scores of page g + 2 (which complete the next phase of this
-                // parity's QKP barrier) wait for it, so no phase is skipped.
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(ctl, B_SEMPTY + par));
                     mbar_arrive_cluster_relaxed(mapa(bar(ctl, B_SEMPTY + par), peer));
                 }
-                uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                const uint32_t s_stg = s_stage + s * kStageBytes;
-                const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + s), peer);
-                mbar_arrive_expect_tx(bar(ctl, B_PMSG + s), kMsgBytes);
+                // P half -> this CTA's P tile and the peer's, with (max, row sum), once
+                // both V stages are free (PV of page g - 2 done in both CTAs)
+                if (g >= 2 && (!wait_warp(ctl, bar(ctl, B_VEMPTY + par), ((g >> 1) - 1) & 1) ||
+                               !wait_warp(ctl, bar(ctl, B_VEMPTY_PEER + par), ((g >> 1) - 1) & 1, kSignal))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *vst = smem + kOffV + par * kVStageBytes;
+                const uint32_t s_vst = s_v + par * kVStageBytes;
+                const uint32_t r_vst = mapa(s_vst, peer);   // the peer's V stage (same layout)
+                const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + par), peer);
+                uint32_t poff[4];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t off = h * 128 + ((((4 * rank + cc) ^ (h & 7))) << 4);
-                    const uint4 v = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                    *reinterpret_cast<uint4 *>(stage + 4 * rank * kBox + off) = v;
-                    st_async_v4_b32(mapa(s_stg + 4 * peer * kBox + off, peer), v, pmsg_peer);
-                }
-                {
-                    const uint32_t off = kSlotRope * kBox + rank * 1024 + h * 8;
-                    *reinterpret_cast<float2 *>(stage + off) = make_float2(m_used, l_own);
-                    st_async_v2_f32(mapa(s_stg + off, peer), m_used, l_own, pmsg_peer);
-                }
-                if (valid < kPage) {
-                    // zero this CTA's latent rows of the masked tail (own and peer tokens)
-                    // so that 0 * garbage stays 0 in PV
-                    const int v_peer = min(max(valid - kHalfTok * (int)peer, 0), kHalfTok);
-                    const int n_own = (kHalfTok - v_own) * 8 * 4, n_peer = (kHalfTok - v_peer) * 8 * 4;
-                    for (int idx = h; idx < n_own + n_peer; idx += 128) {
-                        const bool o = idx < n_own;
-                        const int x = o ? idx : idx - n_own;
-                        const int per_blk = (kHalfTok - (o ? v_own : v_peer)) * 8;
-                        const int blk = x / per_blk, rem = x % per_blk;
-                        const int tok = (o ? v_own : v_peer) + rem / 8;
-                        const uint32_t slot = (o ? kSlotOwnV : 4 * peer) + blk;
-                        *reinterpret_cast<uint4 *>(stage + slot * kBox + tok * 128 + (rem % 8) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                }
+                for (int cc = 0; cc < 4; ++cc) poff[cc] = kVP + h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4);
+                const uint32_t moff = kVMsg + rank * 1024 + h * 8;
+                // local copy first, made visible to the tensor cores before the
+                // (slower) remote copy goes out
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(vst + poff[cc]) =
+                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                *reinterpret_cast<float2 *>(vst + moff) = make_float2(m_used, l_own);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + s));
+                if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + par));
+                mbar_arrive_expect_tx(bar(ctl, B_PMSG + par), kMsgBytes);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    st_async_v4_b32(r_vst + poff[cc],
+                                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]),
+                                    pmsg_peer);
+                st_async_v2_f32(r_vst + moff, m_used, l_own, pmsg_peer);
             }
         }
     } else {
@@ -637,6 +630,26 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_off + kColO;
         const float NEG_INF = -INFINITY;
+        const bool vring = warp == kMergeWarp0;
+        // V ring load of page gv (warp 8): both token halves of this CTA's output
+        // dims, once PV of page gv - 2 freed the stage
+        auto load_v = [&](uint32_t gv, int page) -> bool {
+            const uint32_t p = gv & 1;
+            if (gv >= 2 && !wait_warp(ctl, bar(ctl, B_VEMPTY + p), ((gv >> 1) - 1) & 1)) return false;
+            if (lane == 0) {
+                const uint32_t fv = bar(ctl, B_VFULL + p);
+                const uint32_t dst = s_v + p * kVStageBytes;
+                mbar_arrive_expect_tx(fv, 8 * kBox);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int blk = 4 * (int)rank + j;
+                    tma_load_3d(dst + kVOwn + j * kBox, &P.tm_kv, 64 * blk, tok_own, page, fv);
+                    tma_load_3d(dst + kVPeer + j * kBox, &P.tm_kv, 64 * blk, tok_peer, page, fv);
+                }
+            }
+            __syncwarp();
+            return true;
+        };
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -644,6 +657,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int b = it.row / P.s_q;
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
+            const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
             // q dims 192-383 of this head -> TMEM (for later items this happens
             // before the previous item's epilogue, so that their scores overlap it)
@@ -653,6 +667,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
             }
+            const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
+            int next_first = 0;   // first page of the next item (for the V ring)
+            if (vring && i + 1 < i_end) {
+                const WorkItem nx = items[i + 1];
+                next_first = P.block_table[(size_t)(nx.row / P.s_q) * P.max_pages + nx.kv_begin / kPage];
+            }
+            if (vring && ii == 0 && !load_v(g, bt[0])) break;
             // every page of the item must lie in the pool
             bool bad = false;
             for (int k0 = 0; k0 < n; k0 += 32) {
@@ -666,17 +687,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             // running row sum, so the sums are combined once, at the last page.
             float m_ref = NEG_INF, l_run = 0.f;
             for (int k = 0; k < n; ++k) {
-                const uint32_t gp = g + k, par = gp & 1, s = gp % kStages;
-                if (!wait_warp(ctl, bar(ctl, B_SDONE + s), (gp / kStages) & 1) ||
-                    !wait_warp(ctl, bar(ctl, B_PMSG + s), (gp / kStages) & 1, kCluster)) {
+                const uint32_t gp = g + k, par = gp & 1;
+                const bool v_next = vring && (k + 1 < n || i + 1 < i_end);
+                const int v_page = !v_next ? 0 : (k + 1 < n ? bt[k + 1] : next_first);
+                if (!wait_warp(ctl, bar(ctl, B_SDONE + par), (gp >> 1) & 1) ||
+                    !wait_warp(ctl, bar(ctl, B_PMSG + par), (gp >> 1) & 1, kCluster)) {
                     ok = false;
                     break;
                 }
-                uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                const float2 h0 = *reinterpret_cast<const float2 *>(stage + kSlotRope * kBox + h * 8);
-                const float2 h1 = *reinterpret_cast<const float2 *>(stage + kSlotRope * kBox + 1024 + h * 8);
+                uint8_t *vst = smem + kOffV + par * kVStageBytes;
+                const float2 h0 = *reinterpret_cast<const float2 *>(vst + kVMsg + h * 8);
+                const float2 h1 = *reinterpret_cast<const float2 *>(vst + kVMsg + 1024 + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
-                uint8_t *prow = stage + 4 * rank * kBox + h * 128;
+                uint8_t *prow = vst + kVP + h * 128;
                 if (h0.x != NEG_INF && h0.x < nref) scale_p_half(prow, h, 0, fast_exp2(h0.x - nref));
                 if (h1.x != NEG_INF && h1.x < nref) scale_p_half(prow, h, 1, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
@@ -701,18 +724,39 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 }
                 m_ref = nref;
                 oref[par * 128 + h] = m_ref;
-                if (k == n - 1) {   // both halves' row sums, relative to the final max (same order in both CTAs)
+                if (k == n - 1) {
+                    // both halves' row sums, relative to the final max (same order in both CTAs)
                     const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : fast_exp2(h0.x - nref));
                     const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : fast_exp2(h1.x - nref));
                     l_run = h0.y * f0 + h1.y * f1;
+                    if (valid_last < kPage) {
+                        // zero this CTA's latent rows of the masked tail (both token
+                        // halves) once they landed, so that 0 * garbage stays 0 in PV
+                        if (!wait_warp(ctl, bar(ctl, B_VFULL + par), (gp >> 1) & 1)) { ok = false; break; }
+                        const int v0 = min(max(valid_last - tok_own, 0), kHalfTok);
+                        const int v1 = min(max(valid_last - tok_peer, 0), kHalfTok);
+                        const int n0 = (kHalfTok - v0) * 8 * 4, n1 = (kHalfTok - v1) * 8 * 4;
+                        for (int idx = h; idx < n0 + n1; idx += 128) {
+                            const bool o = idx < n0;
+                            const int x = o ? idx : idx - n0;
+                            const int per_blk = (kHalfTok - (o ? v0 : v1)) * 8;
+                            const int blk = x / per_blk, rem = x % per_blk;
+                            const int tok = (o ? v0 : v1) + rem / 8;
+                            *reinterpret_cast<uint4 *>(vst + (o ? kVOwn : kVPeer) + blk * kBox + tok * 128 +
+                                                       (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(ctl, B_RESDONE + par));
-                    mbar_arrive(bar(ctl, B_PREADY + s));
+                    mbar_arrive(bar(ctl, B_PREADY + par));
                 }
+                // the next page's V stage, as soon as PV of the page before this one
+                // released it
+                if (v_next && !load_v(gp + 1, v_page)) { ok = false; break; }
             }
             g += n;
             if (!ok) break;
@@ -726,20 +770,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
 
             // epilogue: wait for the last PV, normalise, store this CTA's half.  The
-            // rows go through the last page's stage (free now: its MMAs are done and
-            // it is only refilled after this epilogue releases it) so that every
+            // rows go through the last page's V stage (free now: its MMAs are done
+            // and it is only refilled after this epilogue releases it) so that every
             // global store writes 256 contiguous bytes of one row.
-            // The item's last PV is done.  (The end command comes before that PV is
-            // issued, so the per-parity PV barriers may already be a phase further:
-            // a barrier with one phase per item keeps the wait exact.)
             if (!wait_warp(ctl, bar(ctl, B_PVLAST), ii & 1)) break;
             tc_fence_after();
-            const float o_ref = m_ref;
-            const uint32_t s_last = (g - 1) % kStages;
-            uint8_t *lstage = smem + kOffStage + s_last * kStageBytes;
+            const uint32_t p_last = (g - 1) & 1;
+            uint8_t *lstage = smem + kOffV + p_last * kVStageBytes;
             const float nan = __int_as_float(0x7fc00000);
             const float inv = bad ? nan : 1.f / l_run;
-            const float lse = bad ? nan : (o_ref + log2f(l_run)) * 0.69314718055994531f;
+            const float lse = bad ? nan : (m_ref + log2f(l_run)) * 0.69314718055994531f;
             uint8_t *stg = lstage + quarter * 8192;   // 32 rows x 256 B
             uint8_t *my_stg = stg + lane * 256;
             const bool final_out = it.part < 0;
@@ -813,8 +853,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             if (warp == kMergeWarp0) {
                 if (!wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
                 if (lane == 0) {
-                    mbar_arrive(bar(ctl, B_EMPTY_OWN + s_last));
-                    mbar_arrive_cluster(mapa(bar(ctl, B_EMPTY_PEER + s_last), peer));
+                    mbar_arrive(bar(ctl, B_VEMPTY + p_last));
+                    mbar_arrive_cluster(mapa(bar(ctl, B_VEMPTY_PEER + p_last), peer));
                 }
             }
         }
