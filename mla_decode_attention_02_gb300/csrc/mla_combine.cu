@@ -28,6 +28,10 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
                    float *__restrict__ lse_out, int32_t batch, int32_t s_q, int32_t num_units) {
     // launched as a programmatic dependent of the main kernel
     ptx::pdl_wait_prior();
+    // nothing to merge when no row was split and every row was valid: the main
+    // kernel wrote every output itself
+    const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(ws);
+    if (hdr->num_parts == 0 && (hdr->status & MLA_DEV_BAD_SEQ_LEN) == 0) return;
     const PlanLayout L = plan_layout(batch, s_q, num_units);
     const int32_t lane = threadIdx.x & 31;
     const int64_t tasks = (int64_t)L.num_rows * kHeads;

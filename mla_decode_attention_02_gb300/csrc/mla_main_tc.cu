@@ -14,37 +14,37 @@
 // tokens [32c, 32c + 32) of every 64-token page.
 //
 //   S_c = q . k_c^T     tcgen05 M=128 (heads) N=32 (own tokens) K=576, fp32
-//                       in TMEM; q dims 0-383 are the A operand in TMEM,
-//                       384-575 in shared memory
-//   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, written into
-//                       this CTA's P tile and the peer's (st.async, 8 KB)
+//                       in TMEM; q dims 0-447 are the A operand in TMEM,
+//                       448-575 in shared memory
+//   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, into this CTA's
+//                       P slot; the merge warps copy it into the peer's
+//                       (st.async, 8 KB per page)
 //   merge: the pair agrees on the running max per head (each side's max
 //          travels with its P half; the lower half is scaled) and rescales
 //          O when the max grows; each half's running row sum rides along
 //   O_c += [P_0 | P_1] . V_c   tcgen05 M=128 N=256 K=64, V_c = the page's
 //                       latent dims [256c, 256c + 256) of all 64 tokens
 //
-// Two page rings.  The K ring holds this CTA's 32 tokens of a page (all 576
-// dims, 36 KB) and is released as soon as the score MMAs are done; the V
-// ring holds the page's 64 tokens of this CTA's 256 output dims (32 KB, own
-// tokens loaded a second time, from L2), the P tile and the two halves'
-// messages, and is released by PV.  The score chain (load -> MMA) thus never
-// waits for the softmax, the exchange or PV of earlier pages.
+// Three rings, so that no stage waits for a later one: the K ring (this
+// CTA's 32 tokens of a page, all 576 dims, 36 KB) is freed by the score
+// MMAs; the V ring (the page's 64 tokens of this CTA's 256 output dims,
+// 32 KB; own tokens loaded a second time, from L2) and the P ring (the two
+// halves' P tiles and messages, 18 KB, three slots) are freed by PV.
 //
-// Measured on this part: one SM's shared memory streams about 250 GB/s, and
-// scoring only the own half keeps the traffic near 220 KB per page and SM;
-// distributed shared memory moves only 15-20 GB/s per SM, which the 8 KB P
-// half per page fits.
+// Measured on this part: one SM's shared memory streams about 250 GB/s;
+// the pair's distributed-shared-memory link about 27 GB/s per direction,
+// 0.34 us for a page's P half and messages, so the copy is issued by the
+// merge warps, away from the softmax loop.
 //
-// TMEM (512 columns): O half [0,256), S (two pages) [256,320), q [320,512).
-// Warp roles per CTA: warp 0 loads the K ring and q; warps 1 and 2 issue
-// the score products of even and odd pages and warp 3 the PV product (each a
-// whole warp that waits together and issues from one elected lane: about
-// 15 ns per tcgen05.mma, against 35 ns from a lane-0 branch); warps 4-7 (one
-// per TMEM lane quarter, one thread per head) load q into TMEM and compute P;
-// warps 8-11 merge the two halves and run the epilogue, and warp 8 loads the
-// V ring (page g + 1 as soon as page g is merged).  Every wait is bounded: on time-out the kernel records
-// MLA_DEV_TIMEOUT and winds down instead of hanging.
+// TMEM (512 columns): O half [0,256), S [256,288), q [288,512).  Warp roles
+// per CTA: warp 0 loads the K ring and q, warp 2 the V ring; warp 1 issues
+// the score MMAs and warp 3 the PV MMAs (each a whole warp that waits
+// together and issues from one elected lane: about 15 ns per tcgen05.mma,
+// against 35 ns from a lane-0 branch); warps 4-7 (one per TMEM lane quarter,
+// one thread per head) load q into TMEM and compute P; warps 8-11 send P,
+// merge the two halves and run the epilogue.  Every wait is bounded: on
+// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
+// hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -61,69 +61,76 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 384;
-constexpr int kQkWarp0 = 1;         // warps 1, 2: score MMAs of even, odd pages
+constexpr int kQkWarp = 1;          // score MMAs (and TMEM allocation)
+constexpr int kVWarp = 2;           // V ring loads
 constexpr int kPvWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;    // warps 4-7
 constexpr int kMergeWarp0 = 8;      // warps 8-11
-constexpr int kKStages = 2;         // K ring (indexed by page parity)
-constexpr int kVStages = 2;         // V ring (indexed by page parity)
+constexpr int kKStages = 2;         // K ring (page parity)
+constexpr int kVStages = 2;         // V ring (page parity)
+constexpr int kPSlots = 3;          // P ring (page mod 3)
 constexpr int kPrefetch = 3;        // L2 prefetch distance in pages
 constexpr int kClusterSize = 2;
 constexpr uint16_t kBoth = 0x3;
 constexpr int kHalfTok = 32;                      // tokens of a page per CTA
 constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-byte swizzle
 constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8
+constexpr uint32_t kVStageBytes = 8 * kBox;       // own, then peer tokens; output dims
+constexpr uint32_t kVOwn = 0, kVPeer = 4 * kBox;
+constexpr uint32_t kPTileBytes = 128 * 128;       // 128 heads x 64 tokens, bf16, 128-byte swizzle
+constexpr uint32_t kPMsg = kPTileBytes;           // (max, row sum) per head, 1 KB per CTA
+constexpr uint32_t kPSlotBytes = kPTileBytes + 2048;
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
-constexpr int kQTDims = 384;                      // q dims 0-383 live in TMEM
-constexpr uint32_t kQSBytes = 3 * kQBlk;          // q dims 384-575 in shared memory
-// V stage: own tokens' output dims, peer tokens' output dims, P tile, messages
-constexpr uint32_t kVOwn = 0, kVPeer = 4 * kBox, kVP = 8 * kBox, kVMsg = 12 * kBox;
-constexpr uint32_t kVStageBytes = kVMsg + 2048;
+constexpr int kQTDims = 448;                      // q dims 0-447 live in TMEM
+constexpr uint32_t kQSBytes = 2 * kQBlk;          // q dims 448-575 in shared memory
+constexpr int kRefLag = 4;          // the softmax of page g starts from the agreed max of page g - 4
 constexpr uint32_t kOffQS = 0;
 constexpr uint32_t kOffK = kQSBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kKStageBytes;
-constexpr uint32_t kOffRef = kOffV + kVStages * kVStageBytes;  // agreed max, 2 x 128 floats
-constexpr uint32_t kOffBar = kOffRef + 1024;
+constexpr uint32_t kOffP = kOffV + kVStages * kVStageBytes;
+constexpr uint32_t kOffRef = kOffP + kPSlots * kPSlotBytes;   // agreed max, kRefLag x 128 floats
+constexpr uint32_t kOffBar = kOffRef + kRefLag * 512;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers, + alignment slack
-static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kOffV % 1024 == 0 &&
-                  kVStageBytes % 1024 == 0,
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 &&
+                  kKStageBytes % 1024 == 0 && kVStageBytes % 1024 == 0 && kPSlotBytes % 1024 == 0,
               "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, row sum)
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
-constexpr uint32_t kColS = 256;     // 2 x 32 fp32 scores (pages of even / odd index)
-constexpr uint32_t kColQ = 320;     // 192 columns of packed bf16 q (dims 0-383)
+constexpr uint32_t kColS = 256;     // 32 fp32 scores
+constexpr uint32_t kColQ = 288;     // 224 columns of packed bf16 q (dims 0-447)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: raise the max only when it grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
-// barrier slots (8 bytes each) in the barrier area; "+ p" = page parity
+// barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
     B_Q_FULL = 0,                        // producer (+tx), softmax and merge warps (q in TMEM)
-    B_Q_EMPTY = 1,                       // both score issuers of both CTAs done with q
-    B_KFULL = 2,                         // + p: dim blocks 0-5 of the K stage landed (+tx)
-    B_KFULLB = B_KFULL + 2,              // + p: blocks 6-8 landed (+tx)
-    B_KEMPTY = B_KFULLB + 2,             // + p: score MMAs done with the K stage
-    B_VFULL = B_KEMPTY + 2,              // + p: V stage landed (+tx)
-    B_VEMPTY = B_VFULL + 2,              // + p: this CTA's PV done with the V stage
-    B_VEMPTY_PEER = B_VEMPTY + 2,        // + p: the peer's PV done with its V stage
-    B_SFULL = B_VEMPTY_PEER + 2,         // + p: scores in TMEM
-    B_QKP = B_SFULL + 2,                 // + p: the peer's scores done
-    B_SEMPTY = B_QKP + 2,                // + p: scores read and the peer's seen, both CTAs
-    B_SDONE = B_SEMPTY + 2,              // + p: own P half written
-    B_PMSG = B_SDONE + 2,                // + p: the peer's P half arrived (+tx)
-    B_PREADY = B_PMSG + 2,               // + p: P tile final, PV may run
-    B_RESDONE = B_PREADY + 2,            // + p: agreed max published
-    B_PVDONE = B_RESDONE + 2,            // + p: PV done
+    B_Q_EMPTY = 1,                       // score issuers of both CTAs done with q
+    B_KFULL = 2,                         // + page parity: dim blocks 0-6 landed (+tx)
+    B_KFULLB = B_KFULL + 2,              // + page parity: blocks 7-8 landed (+tx)
+    B_KEMPTY = B_KFULLB + 2,             // + page parity: score MMAs done with the K stage
+    B_VFULL = B_KEMPTY + 2,              // + page parity: V stage landed (+tx)
+    B_VEMPTY = B_VFULL + 2,              // + page parity: PV done with the V stage
+    B_PEMPTY = B_VEMPTY + 2,             // + slot: this CTA's PV done with the P slot
+    B_PEMPTY_PEER = B_PEMPTY + kPSlots,  // + slot: the peer's PV done with its P slot
+    B_SFULL = B_PEMPTY_PEER + kPSlots,   // scores in TMEM
+    B_QKP = B_SFULL + 1,                 // the peer's scores done
+    B_SEMPTY = B_QKP + 1,                // scores read and the peer's seen, both CTAs
+    B_SDONE = B_SEMPTY + 1,              // + slot: own P half written
+    B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx)
+    B_PREADY = B_PMSG + kPSlots,         // + slot: P tile final, PV may run
+    B_RESDONE = B_PREADY + kPSlots,      // + page mod kRefLag: agreed max published
+    B_PVDONE = B_RESDONE + kRefLag,      // + page parity: PV done
     B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
-    B_DRAIN = B_EPI + 1,                 // + issuer (0, 1: score, 2: PV)
-    B_COUNT = B_DRAIN + 3,
+    B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
+    B_COUNT = B_DRAIN + 2,
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 
@@ -223,16 +230,17 @@ __device__ __forceinline__ void scale_p_half(uint8_t *prow, int h, int half, flo
     }
 }
 
-// q dims [192 part, 192 part + 192) of one head -> TMEM (96 columns).  All
-// 24 loads are in flight before the first store, so an item's q costs one
-// memory round trip rather than one per 64 dims.
-__device__ __forceinline__ void load_q_part(const __nv_bfloat16 *q_row, uint32_t tq, int part) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(q_row) + part * 24;
-    uint4 x[24];
+// q dims [64 c0, 64 (c0 + N)) of one head -> TMEM columns [32 c0, 32 (c0 + N)).
+// All loads are in flight before the first store, so N chunks cost one memory
+// round trip.
+template <int N>
+__device__ __forceinline__ void load_q_chunks(const __nv_bfloat16 *q_row, uint32_t tq, int c0) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(q_row) + c0 * 8;
+    uint4 x[8 * N];
 #pragma unroll
-    for (int v = 0; v < 24; ++v) x[v] = src[v];
+    for (int v = 0; v < 8 * N; ++v) x[v] = src[v];
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
+    for (int c = 0; c < N; ++c) {
         uint32_t q[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -241,7 +249,7 @@ __device__ __forceinline__ void load_q_part(const __nv_bfloat16 *q_row, uint32_t
             q[4 * v + 2] = x[c * 8 + v].z;
             q[4 * v + 3] = x[c * 8 + v].w;
         }
-        tmem_st32(tq + (part * 3 + c) * 32, q);
+        tmem_st32(tq + (c0 + c) * 32, q);
     }
     tmem_wait_st();
 }
@@ -255,7 +263,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     const uint32_t s_qs = s_base + kOffQS;
     const uint32_t s_k = s_base + kOffK;
     const uint32_t s_v = s_base + kOffV;
-    float *oref = reinterpret_cast<float *>(smem + kOffRef);  // [page parity][head]
+    const uint32_t s_p = s_base + kOffP;
+    float *oref = reinterpret_cast<float *>(smem + kOffRef);  // [page mod kRefLag][head]
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -274,27 +283,30 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(bar(ctl, B_Q_FULL), 1 + 8);
-        mbar_init(bar(ctl, B_Q_EMPTY), 2 * kClusterSize);
+        mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_KFULL + p), 1);
             mbar_init(bar(ctl, B_KFULLB + p), 1);
             mbar_init(bar(ctl, B_KEMPTY + p), 1);
             mbar_init(bar(ctl, B_VFULL + p), 1);
             mbar_init(bar(ctl, B_VEMPTY + p), 1);
-            mbar_init(bar(ctl, B_VEMPTY_PEER + p), 1);
-            mbar_init(bar(ctl, B_SFULL + p), 1);
-            mbar_init(bar(ctl, B_QKP + p), 1);
-            mbar_init(bar(ctl, B_SEMPTY + p), 2 * 4);
-            mbar_init(bar(ctl, B_SDONE + p), 4);
-            mbar_init(bar(ctl, B_PMSG + p), 128);
-            mbar_init(bar(ctl, B_PREADY + p), 4);
-            mbar_init(bar(ctl, B_RESDONE + p), 4);
             mbar_init(bar(ctl, B_PVDONE + p), 1);
         }
+        for (int s = 0; s < kPSlots; ++s) {
+            mbar_init(bar(ctl, B_PEMPTY + s), 1);
+            mbar_init(bar(ctl, B_PEMPTY_PEER + s), 1);
+            mbar_init(bar(ctl, B_SDONE + s), 4);
+            mbar_init(bar(ctl, B_PMSG + s), 128);
+            mbar_init(bar(ctl, B_PREADY + s), 4);
+        }
+        mbar_init(bar(ctl, B_SFULL), 1);
+        mbar_init(bar(ctl, B_QKP), 1);
+        mbar_init(bar(ctl, B_SEMPTY), 2 * 4);
+        for (int r = 0; r < kRefLag; ++r) mbar_init(bar(ctl, B_RESDONE + r), 4);
         mbar_init(bar(ctl, B_PVLAST), 1);
         mbar_init(bar(ctl, B_OFREE), 4);
         mbar_init(bar(ctl, B_EPI), 4);
-        for (int d = 0; d < 3; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
+        for (int d = 0; d < 2; ++d) mbar_init(bar(ctl, B_DRAIN + d), 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -302,7 +314,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         prefetch_tmap(&P.tm_q_rope);
         prefetch_tmap(&P.tm_kv);
     }
-    if (warp == kQkWarp0) {
+    if (warp == kQkWarp) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -333,10 +345,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     }
     const int tok_own = kHalfTok * (int)rank, tok_peer = kHalfTok * (int)peer;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ K ring producer
-        // This CTA's tokens of each page (all dims) and q.  Out-of-pool page
+    if (warp == 0 || warp == kVWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // Warp 0: K ring (this CTA's tokens, all dims) and q; warp 2: V ring
+        // (both token halves of this CTA's output dims).  Out-of-pool page
         // indices read zeros (TMA bounds fill); the merge warps flag the row.
+        const bool kring = warp == 0;
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -354,87 +368,102 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const int page = __shfl_sync(0xffffffffu, mine, kk);
                     const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
                     const uint32_t p = g & 1;
-                    if (g >= 2 && !wait_warp(ctl, bar(ctl, B_KEMPTY + p), ((g >> 1) - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        // blocks 0-5 (score MMAs with q in TMEM) and 6-8 complete
-                        // separate barriers, so those MMAs start before the rest lands
-                        const uint32_t fa = bar(ctl, B_KFULL + p), fb = bar(ctl, B_KFULLB + p);
-                        const uint32_t dst = s_k + p * kKStageBytes;
-                        mbar_arrive_expect_tx(fa, 6 * kBox);
-                        mbar_arrive_expect_tx(fb, 3 * kBox);
-#pragma unroll
-                        for (int blk = 0; blk < 9; ++blk)
-                            tma_load_3d(dst + blk * kBox, &P.tm_kv, 64 * blk, tok_own, page,
-                                        blk < 6 ? fa : fb);
-                    }
-                    if (k0 + kk == 0) {
-                        // q dims 384-575, once the first page is on its way: both CTAs'
-                        // copies must be free (last score MMAs of the previous item done)
-                        if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
+                    if (kring) {
+                        if (g >= 2 && !wait_warp(ctl, bar(ctl, B_KEMPTY + p), ((g >> 1) - 1) & 1)) {
                             ok = false;
                             break;
                         }
                         if (lane == 0) {
-                            const uint32_t fb = bar(ctl, B_Q_FULL);
-                            mbar_arrive_expect_tx(fb, kQSBytes);
-                            const int y = it.row * kHeads;
-                            if (rank == 0) {
-                                tma_load_2d_mc(s_qs, &P.tm_q_lat, kQTDims, y, fb, kBoth);
-                                tma_load_2d_mc(s_qs + kQBlk, &P.tm_q_lat, kQTDims + 64, y, fb, kBoth);
-                            } else {
-                                tma_load_2d_mc(s_qs + 2 * kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                            // blocks 0-6 (score MMAs with q in TMEM) and 7-8 complete
+                            // separate barriers, so those MMAs start before the rest lands
+                            const uint32_t fa = bar(ctl, B_KFULL + p), fb = bar(ctl, B_KFULLB + p);
+                            const uint32_t dst = s_k + p * kKStageBytes;
+                            mbar_arrive_expect_tx(fa, 7 * kBox);
+                            mbar_arrive_expect_tx(fb, 2 * kBox);
+#pragma unroll
+                            for (int blk = 0; blk < 9; ++blk)
+                                tma_load_3d(dst + blk * kBox, &P.tm_kv, 64 * blk, tok_own, page,
+                                            blk < 7 ? fa : fb);
+                        }
+                        if (k0 + kk == 0) {
+                            // q dims 448-575, once the first page is on its way: both
+                            // CTAs' copies must be free (last score MMAs of the previous
+                            // item done)
+                            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
+                                ok = false;
+                                break;
+                            }
+                            if (lane == 0) {
+                                const uint32_t fb = bar(ctl, B_Q_FULL);
+                                mbar_arrive_expect_tx(fb, kQSBytes);
+                                const int y = it.row * kHeads;
+                                if (rank == 0)
+                                    tma_load_2d_mc(s_qs, &P.tm_q_lat, kQTDims, y, fb, kBoth);
+                                else
+                                    tma_load_2d_mc(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                            }
+                        }
+                        // warm L2 for a page beyond the ones in flight (each CTA warms
+                        // its own token half, which the peer's V ring reads as well)
+                        if (lane == 0 && k0 + kk + kPrefetch < n)
+                            for (int blk = 0; blk < 9; ++blk)
+                                tma_prefetch_3d(&P.tm_kv, 64 * blk, tok_own, page_ahead);
+                    } else {
+                        if (g >= 2 && !wait_warp(ctl, bar(ctl, B_VEMPTY + p), ((g >> 1) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            const uint32_t fv = bar(ctl, B_VFULL + p);
+                            const uint32_t dst = s_v + p * kVStageBytes;
+                            mbar_arrive_expect_tx(fv, kVStageBytes);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int blk = 4 * (int)rank + j;
+                                tma_load_3d(dst + kVOwn + j * kBox, &P.tm_kv, 64 * blk, tok_own, page, fv);
+                                tma_load_3d(dst + kVPeer + j * kBox, &P.tm_kv, 64 * blk, tok_peer, page, fv);
                             }
                         }
                     }
-                    // warm L2 for a page beyond the ones in flight (each CTA warms its
-                    // own token half, which the peer's V ring reads as well)
-                    if (lane == 0 && k0 + kk + kPrefetch < n)
-                        for (int blk = 0; blk < 9; ++blk)
-                            tma_prefetch_3d(&P.tm_kv, 64 * blk, tok_own, page_ahead);
                     __syncwarp();
                 }
             }
         }
-    } else if (warp == kQkWarp0 || warp == kQkWarp0 + 1 || warp == kPvWarp) {
+    } else if (warp == kQkWarp || warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuers
         // The whole warp runs the schedule and waits; one elected lane issues.
-        const int role = warp - kQkWarp0;   // 0, 1: score MMAs of even / odd pages; 2: PV
+        const bool qk = warp == kQkWarp;
         // Descriptor bases; every MMA below adds a byte offset (>> 4).
         const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
         const uint64_t d_k = smem_desc(s_k, 16, 1024, 2);
-        const uint64_t d_p = smem_desc(s_v + kVP, 16, 1024, 2);
+        const uint64_t d_p = smem_desc(s_p, 16, 1024, 2);
         const uint64_t d_vown = smem_desc(s_v + kVOwn, 4096, 1024, 2);
         const uint64_t d_vpeer = smem_desc(s_v + kVPeer, 4096, 1024, 2);
         constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
         constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
-        const uint32_t tQ = tmem + kColQ, tO = tmem + kColO;
+        const uint32_t tQ = tmem + kColQ, tO = tmem + kColO, tS = tmem + kColS;
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            // every score issuer takes part in every item's q hand-over, pages or not
-            if (role < 2 && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+            if (qk && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
             for (int k = 0; k < n && ok; ++k, ++g) {
                 const uint32_t p = g & 1;
-                if (role < 2) {
-                    if ((int)p != role) continue;
+                if (qk) {
+                    // S = q . k_own^T into the single score buffer, once the softmax
+                    // has read the previous page's scores
                     const uint32_t ko = p * kKStageBytes;
                     if (!wait_warp(ctl, bar(ctl, B_KFULL + p), (g >> 1) & 1)) { ok = false; break; }
-                    if (g >= 2 &&
-                        !wait_warp(ctl, bar(ctl, B_SEMPTY + p), ((g >> 1) - 1) & 1, kSignal)) {
+                    if (g >= 1 && !wait_warp(ctl, bar(ctl, B_SEMPTY), (g - 1) & 1, kSignal)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t tS = tmem + kColS + kHalfTok * p;
                     if (elect_one()) {
 #pragma unroll
-                        for (int ks = 0; ks < 24; ++ks)
+                        for (int ks = 0; ks < 28; ++ks)
                             mma_ts(tS, tQ + 8 * ks,
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, ks > 0 ? 1u : 0u);
@@ -444,21 +473,22 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
-                        for (int ks = 24; ks < 36; ++ks)
-                            mma_ss(tS, d_qs + (uint64_t)((((ks - 24) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
+                        for (int ks = 28; ks < 36; ++ks)
+                            mma_ss(tS, d_qs + (uint64_t)((((ks - 28) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, 1u);
-                        mma_commit(bar(ctl, B_SFULL + p));
-                        mma_commit_mc(bar(ctl, B_QKP + p), peer_mask);
+                        mma_commit(bar(ctl, B_SFULL));
+                        mma_commit_mc(bar(ctl, B_QKP), peer_mask);
                         mma_commit(bar(ctl, B_KEMPTY + p));
                     }
                     __syncwarp();
                 } else {
                     // O_c (+)= [P_0 | P_1] . V_c once the V stage landed and the merge
-                    // warps released the P tile
-                    const uint32_t vo = p * kVStageBytes;
+                    // warps released the P slot
+                    const uint32_t ps = g % kPSlots, pu = g / kPSlots;
+                    const uint32_t vo = p * kVStageBytes, po = ps * kPSlotBytes;
                     if (!wait_warp(ctl, bar(ctl, B_VFULL + p), (g >> 1) & 1) ||
-                        !wait_warp(ctl, bar(ctl, B_PREADY + p), (g >> 1) & 1)) {
+                        !wait_warp(ctl, bar(ctl, B_PREADY + ps), pu & 1)) {
                         ok = false;
                         break;
                     }
@@ -471,32 +501,32 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint64_t vb = (uint32_t)(ks >> 1) == rank ? d_vown : d_vpeer;
-                            mma_ss(tO, d_p + (uint64_t)((vo + ks * 32) >> 4),
+                            mma_ss(tO, d_p + (uint64_t)((po + ks * 32) >> 4),
                                    vb + (uint64_t)((vo + (ks & 1) * 2048) >> 4), id_pv,
                                    (k == 0 && ks == 0) ? 0u : 1u);
                         }
                         mma_commit(bar(ctl, B_PVDONE + p));
+                        mma_commit(bar(ctl, B_PEMPTY + ps));
+                        mma_commit_mc(bar(ctl, B_PEMPTY_PEER + ps), peer_mask);
                         // the last page's V stage is released by the epilogue, which
                         // stages the output through it
-                        if (k != n - 1) {
+                        if (k != n - 1)
                             mma_commit(bar(ctl, B_VEMPTY + p));
-                            mma_commit_mc(bar(ctl, B_VEMPTY_PEER + p), peer_mask);
-                        } else {
+                        else
                             mma_commit(bar(ctl, B_PVLAST));
-                        }
                     }
                     __syncwarp();
                 }
             }
-            // this issuer is done with the item's q (in both CTAs' copies)
-            if (ok && role < 2) {
+            // the score issuer is done with the item's q (in both CTAs' copies)
+            if (ok && qk) {
                 if (elect_one()) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
                 __syncwarp();
             }
         }
         // wind down: every MMA this warp issued completes before TMEM is freed
         if (elect_one()) {
-            const uint32_t drain = bar(ctl, B_DRAIN + role);
+            const uint32_t drain = bar(ctl, B_DRAIN + (qk ? 0 : 1));
             mma_commit(drain);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
@@ -519,30 +549,39 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q dims 0-191 of this head -> TMEM (the previous item's scores are
-            // done); the merge warps load dims 192-383
+            // q dims 0-255 of this head -> TMEM (the previous item's scores are
+            // done); the merge warps load dims 256-447
             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) break;
-            load_q_part(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tQ, 0);
+            {
+                const __nv_bfloat16 *qrow = P.q_latent + ((size_t)it.row * kHeads + h) * kDl;
+                load_q_chunks<2>(qrow, tQ, 0);
+                load_q_chunks<2>(qrow, tQ, 2);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
             float m_prev = NEG_INF;   // max used for this half's previous page
             float l_own = 0.f;        // row sum of this half's tokens so far, relative to m_prev
             for (int k = 0; k < n; ++k, ++g) {
-                const uint32_t par = g & 1;
-                // Start from the pair's agreed max of two pages back (a fixed point
-                // in the schedule, so the result does not depend on timing).  The
+                const uint32_t ps = g % kPSlots;
+                // Start from the pair's agreed max of kRefLag pages back (a fixed
+                // point in the schedule, so the result does not depend on timing;
+                // far enough back that the merge chain never stalls this loop).  The
                 // wait is taken on every page so that no phase of the barrier is
                 // skipped.
                 float base = m_prev;
-                if (g >= 2) {
-                    if (!wait_warp(ctl, bar(ctl, B_RESDONE + par), ((g >> 1) - 1) & 1)) { ok = false; break; }
-                    if (k >= 2) base = fmaxf(base, oref[par * 128 + h]);
+                if (g >= (uint32_t)kRefLag) {
+                    const uint32_t slot = g % kRefLag;
+                    if (!wait_warp(ctl, bar(ctl, B_RESDONE + slot), ((g / kRefLag) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (k >= kRefLag) base = fmaxf(base, oref[slot * 128 + h]);
                 }
-                if (!wait_warp(ctl, bar(ctl, B_SFULL + par), (g >> 1) & 1)) { ok = false; break; }
+                if (!wait_warp(ctl, bar(ctl, B_SFULL), g & 1)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kColS + kHalfTok * par, r);
+                tmem_ld32(tmem + lane_off + kColS, r);
                 tmem_wait_ld();
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
@@ -551,7 +590,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 // the raw scores gives the max); masked tokens (ragged last page)
                 // are -inf
                 const float sc = P.scale_log2;
-                float rmax = -INFINITY;
+                float rmax = NEG_INF;
                 if (v_own == kHalfTok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) rmax = fmaxf(rmax, __uint_as_float(r[j]));
@@ -563,6 +602,17 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                 }
                 const float lm = rmax * sc;
+                // The score buffer is released in both CTAs once the peer's scores of
+                // this page are seen: the peer's scores of page g + 1 (which complete
+                // the next phase of the QKP barrier) wait for it, so no phase is
+                // skipped.
+                if (!wait_warp(ctl, bar(ctl, B_QKP), g & 1, kSignal)) { ok = false; break; }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(ctl, B_SEMPTY));
+                    mbar_arrive_cluster_relaxed(mapa(bar(ctl, B_SEMPTY), peer));
+                }
                 // raise the max only when this half's page exceeds it by > 2^8
                 const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
                 const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : fast_exp2(m_prev - m_used));
@@ -578,49 +628,24 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     pk[j] = pack_bf16(e0, e1);
                 }
                 l_own = l_own * l_scale + rsum;
-                // The score buffer is released in both CTAs once the peer's scores of
-                // this page are seen: the peer's scores of page g + 2 (which complete
-                // the next phase of this parity's QKP barrier) wait for it, so no
-                // phase is skipped.
-                if (!wait_warp(ctl, bar(ctl, B_QKP + par), (g >> 1) & 1, kSignal)) { ok = false; break; }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(ctl, B_SEMPTY + par));
-                    mbar_arrive_cluster_relaxed(mapa(bar(ctl, B_SEMPTY + par), peer));
-                }
-                // P half -> this CTA's P tile and the peer's, with (max, row sum), once
-                // both V stages are free (PV of page g - 2 done in both CTAs)
-                if (g >= 2 && (!wait_warp(ctl, bar(ctl, B_VEMPTY + par), ((g >> 1) - 1) & 1) ||
-                               !wait_warp(ctl, bar(ctl, B_VEMPTY_PEER + par), ((g >> 1) - 1) & 1, kSignal))) {
+                // the P slot is free in both CTAs once PV of page g - kPSlots is done
+                if (g >= (uint32_t)kPSlots &&
+                    (!wait_warp(ctl, bar(ctl, B_PEMPTY + ps), ((g / kPSlots) - 1) & 1) ||
+                     !wait_warp(ctl, bar(ctl, B_PEMPTY_PEER + ps), ((g / kPSlots) - 1) & 1, kSignal))) {
                     ok = false;
                     break;
                 }
-                uint8_t *vst = smem + kOffV + par * kVStageBytes;
-                const uint32_t s_vst = s_v + par * kVStageBytes;
-                const uint32_t r_vst = mapa(s_vst, peer);   // the peer's V stage (same layout)
-                const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + par), peer);
-                uint32_t poff[4];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) poff[cc] = kVP + h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4);
-                const uint32_t moff = kVMsg + rank * 1024 + h * 8;
-                // local copy first, made visible to the tensor cores before the
-                // (slower) remote copy goes out
+                // this half's P row and (max, row sum) -> this CTA's P slot; the merge
+                // warps copy them on into the peer's
+                uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(vst + poff[cc]) =
+                    *reinterpret_cast<uint4 *>(pst + h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                *reinterpret_cast<float2 *>(vst + moff) = make_float2(m_used, l_own);
+                *reinterpret_cast<float2 *>(pst + kPMsg + rank * 1024 + h * 8) = make_float2(m_used, l_own);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + par));
-                mbar_arrive_expect_tx(bar(ctl, B_PMSG + par), kMsgBytes);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    st_async_v4_b32(r_vst + poff[cc],
-                                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]),
-                                    pmsg_peer);
-                st_async_v2_f32(r_vst + moff, m_used, l_own, pmsg_peer);
+                if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + ps));
             }
         }
     } else {
@@ -629,27 +654,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const int h = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_off + kColO;
+        const uint32_t tQ = tmem + lane_off + kColQ;
         const float NEG_INF = -INFINITY;
-        const bool vring = warp == kMergeWarp0;
-        // V ring load of page gv (warp 8): both token halves of this CTA's output
-        // dims, once PV of page gv - 2 freed the stage
-        auto load_v = [&](uint32_t gv, int page) -> bool {
-            const uint32_t p = gv & 1;
-            if (gv >= 2 && !wait_warp(ctl, bar(ctl, B_VEMPTY + p), ((gv >> 1) - 1) & 1)) return false;
-            if (lane == 0) {
-                const uint32_t fv = bar(ctl, B_VFULL + p);
-                const uint32_t dst = s_v + p * kVStageBytes;
-                mbar_arrive_expect_tx(fv, 8 * kBox);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int blk = 4 * (int)rank + j;
-                    tma_load_3d(dst + kVOwn + j * kBox, &P.tm_kv, 64 * blk, tok_own, page, fv);
-                    tma_load_3d(dst + kVPeer + j * kBox, &P.tm_kv, 64 * blk, tok_peer, page, fv);
-                }
-            }
-            __syncwarp();
-            return true;
-        };
         uint32_t g = 0;
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -659,47 +665,50 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
-            // q dims 192-383 of this head -> TMEM (for later items this happens
+            // q dims 256-447 of this head -> TMEM (for later items this happens
             // before the previous item's epilogue, so that their scores overlap it)
             if (ii == 0) {
-                load_q_part(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tmem + lane_off + kColQ, 1);
+                load_q_chunks<3>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tQ, 4);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
             }
-            const int32_t *bt = P.block_table + (size_t)b * P.max_pages + p0;
-            int next_first = 0;   // first page of the next item (for the V ring)
-            if (vring && i + 1 < i_end) {
-                const WorkItem nx = items[i + 1];
-                next_first = P.block_table[(size_t)(nx.row / P.s_q) * P.max_pages + nx.kv_begin / kPage];
-            }
-            if (vring && ii == 0 && !load_v(g, bt[0])) break;
             // every page of the item must lie in the pool
             bool bad = false;
             for (int k0 = 0; k0 < n; k0 += 32) {
                 int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
                 bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
             }
-            // Merge the pair's halves of each page: agree on the max per head (a
-            // half computed against a lower one is scaled; O is rescaled when the
-            // agreed max grows), publish it for the softmax two pages on and
-            // release the P tile to the PV warp.  Each half's message carries its
-            // running row sum, so the sums are combined once, at the last page.
+            // Per page: send this CTA's P half on to the peer, then merge the pair's
+            // halves: agree on the max per head (a half computed against a lower
+            // one is scaled; O is rescaled when the agreed max grows), publish it
+            // for the softmax kRefLag pages on and release the P slot to the PV
+            // warp.  Each half's message carries its running row sum, so the sums
+            // are combined once, at the last page.
             float m_ref = NEG_INF, l_run = 0.f;
             for (int k = 0; k < n; ++k) {
-                const uint32_t gp = g + k, par = gp & 1;
-                const bool v_next = vring && (k + 1 < n || i + 1 < i_end);
-                const int v_page = !v_next ? 0 : (k + 1 < n ? bt[k + 1] : next_first);
-                if (!wait_warp(ctl, bar(ctl, B_SDONE + par), (gp >> 1) & 1) ||
-                    !wait_warp(ctl, bar(ctl, B_PMSG + par), (gp >> 1) & 1, kCluster)) {
-                    ok = false;
-                    break;
+                const uint32_t gp = g + k, par = gp & 1, ps = gp % kPSlots, pu = gp / kPSlots;
+                if (!wait_warp(ctl, bar(ctl, B_SDONE + ps), pu & 1)) { ok = false; break; }
+                uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
+                {
+                    const uint32_t s_pst = s_p + ps * kPSlotBytes;
+                    const uint32_t r_pst = mapa(s_pst, peer);
+                    const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + ps), peer);
+                    mbar_arrive_expect_tx(bar(ctl, B_PMSG + ps), kMsgBytes);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t off = h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4);
+                        st_async_v4_b32(r_pst + off, *reinterpret_cast<const uint4 *>(pst + off), pmsg_peer);
+                    }
+                    const uint32_t moff = kPMsg + rank * 1024 + h * 8;
+                    const float2 mine = *reinterpret_cast<const float2 *>(pst + moff);
+                    st_async_v2_f32(r_pst + moff, mine.x, mine.y, pmsg_peer);
                 }
-                uint8_t *vst = smem + kOffV + par * kVStageBytes;
-                const float2 h0 = *reinterpret_cast<const float2 *>(vst + kVMsg + h * 8);
-                const float2 h1 = *reinterpret_cast<const float2 *>(vst + kVMsg + 1024 + h * 8);
+                if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) { ok = false; break; }
+                const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPMsg + h * 8);
+                const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPMsg + 1024 + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
-                uint8_t *prow = vst + kVP + h * 128;
+                uint8_t *prow = pst + h * 128;
                 if (h0.x != NEG_INF && h0.x < nref) scale_p_half(prow, h, 0, fast_exp2(h0.x - nref));
                 if (h1.x != NEG_INF && h1.x < nref) scale_p_half(prow, h, 1, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
@@ -723,7 +732,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     tmem_wait_st();
                 }
                 m_ref = nref;
-                oref[par * 128 + h] = m_ref;
+                oref[(gp % kRefLag) * 128 + h] = m_ref;
                 if (k == n - 1) {
                     // both halves' row sums, relative to the final max (same order in both CTAs)
                     const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : fast_exp2(h0.x - nref));
@@ -733,6 +742,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         // zero this CTA's latent rows of the masked tail (both token
                         // halves) once they landed, so that 0 * garbage stays 0 in PV
                         if (!wait_warp(ctl, bar(ctl, B_VFULL + par), (gp >> 1) & 1)) { ok = false; break; }
+                        uint8_t *vst = smem + kOffV + par * kVStageBytes;
                         const int v0 = min(max(valid_last - tok_own, 0), kHalfTok);
                         const int v1 = min(max(valid_last - tok_peer, 0), kHalfTok);
                         const int n0 = (kHalfTok - v0) * 8 * 4, n1 = (kHalfTok - v1) * 8 * 4;
@@ -751,19 +761,15 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(ctl, B_RESDONE + par));
-                    mbar_arrive(bar(ctl, B_PREADY + par));
+                    mbar_arrive(bar(ctl, B_RESDONE + gp % kRefLag));
+                    mbar_arrive(bar(ctl, B_PREADY + ps));
                 }
-                // the next page's V stage, as soon as PV of the page before this one
-                // released it
-                if (v_next && !load_v(gp + 1, v_page)) { ok = false; break; }
             }
             g += n;
             if (!ok) break;
             if (i + 1 < i_end) {
                 if (!wait_warp(ctl, bar(ctl, B_Q_EMPTY), ii & 1, kCluster)) break;
-                load_q_part(P.q_latent + ((size_t)items[i + 1].row * kHeads + h) * kDl,
-                            tmem + lane_off + kColQ, 1);
+                load_q_chunks<3>(P.q_latent + ((size_t)items[i + 1].row * kHeads + h) * kDl, tQ, 4);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
@@ -846,16 +852,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 else lse_part[(size_t)it.part * kHeads + h] = lse;
             }
             if (bad && lane == 0 && rank == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
-            // once every merge warp is done with the stage, release it in both CTAs
+            // once every merge warp is done with the stage, release it
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
             if (warp == kMergeWarp0) {
                 if (!wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
-                if (lane == 0) {
-                    mbar_arrive(bar(ctl, B_VEMPTY + p_last));
-                    mbar_arrive_cluster(mapa(bar(ctl, B_VEMPTY_PEER + p_last), peer));
-                }
+                if (lane == 0) mbar_arrive(bar(ctl, B_VEMPTY + p_last));
             }
         }
     }
@@ -864,7 +867,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     tc_fence_before();
     __syncthreads();
     cluster_sync();
-    if (warp == kQkWarp0) {
+    if (warp == kQkWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
