@@ -17,8 +17,8 @@
 //                       in TMEM; q dims 0-447 are the A operand in TMEM,
 //                       448-575 in shared memory
 //   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, into this CTA's
-//                       P slot; the merge warps copy it into the peer's
-//                       (st.async, 8 KB per page)
+//                       P slot; one bulk copy (issued by a merge warp) puts
+//                       it into the peer's (9 KB per page)
 //   merge: the pair agrees on the running max per head (each side's max
 //          travels with its P half; the lower half is scaled) and rescales
 //          O when the max grows; each half's running row sum rides along
@@ -33,8 +33,9 @@
 //
 // Measured on this part: one SM's shared memory streams about 250 GB/s;
 // the pair's distributed-shared-memory link about 27 GB/s per direction,
-// 0.34 us for a page's P half and messages, so the copy is issued by the
-// merge warps, away from the softmax loop.
+// 0.34 us for a page's P half and messages (twice that while both SMs'
+// shared memory is busy), so it goes as one asynchronous bulk copy that no
+// warp waits on.
 //
 // TMEM (512 columns): O half [0,256), S [256,288), q [288,512).  Warp roles
 // per CTA: warp 0 loads the K ring and q, warp 2 the V ring; warp 1 issues
@@ -77,9 +78,10 @@ constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-by
 constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8
 constexpr uint32_t kVStageBytes = 8 * kBox;       // own, then peer tokens; output dims
 constexpr uint32_t kVOwn = 0, kVPeer = 4 * kBox;
-constexpr uint32_t kPTileBytes = 128 * 128;       // 128 heads x 64 tokens, bf16, 128-byte swizzle
-constexpr uint32_t kPMsg = kPTileBytes;           // (max, row sum) per head, 1 KB per CTA
-constexpr uint32_t kPSlotBytes = kPTileBytes + 2048;
+constexpr uint32_t kPHalf = 128 * 64;             // one token half: 128 heads x 32 tokens, bf16,
+                                                  // 64-byte swizzle; tile c = CTA c's tokens
+constexpr uint32_t kPMsg = 2 * kPHalf;            // (max, row sum) per head, 1 KB per CTA
+constexpr uint32_t kPSlotBytes = 2 * kPHalf + 2048;
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
 constexpr int kQTDims = 448;                      // q dims 0-447 live in TMEM
 constexpr uint32_t kQSBytes = 2 * kQBlk;          // q dims 448-575 in shared memory
@@ -95,7 +97,7 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 &&
                   kKStageBytes % 1024 == 0 && kVStageBytes % 1024 == 0 && kPSlotBytes % 1024 == 0,
               "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kMsgBytes = 64 + 8;            // per head and page: P half + (max, row sum)
+constexpr uint32_t kMsgBytes = kPHalf + 1024;     // per page: P half tile + (max, row sum) per head
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
@@ -124,7 +126,8 @@ enum : uint32_t {
     B_SDONE = B_SEMPTY + 1,              // + slot: own P half written
     B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx)
     B_PREADY = B_PMSG + kPSlots,         // + slot: P tile final, PV may run
-    B_RESDONE = B_PREADY + kPSlots,      // + page mod kRefLag: agreed max published
+    B_PREAD = B_PREADY + kPSlots,        // + slot: the copy to the peer has read this CTA's half
+    B_RESDONE = B_PREAD + kPSlots,       // + page mod kRefLag: agreed max published
     B_PVDONE = B_RESDONE + kRefLag,      // + page parity: PV done
     B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
@@ -213,11 +216,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Scale the four 16-byte chunks of one P row half (bf16) by f.
-__device__ __forceinline__ void scale_p_half(uint8_t *prow, int h, int half, float f) {
+// Byte offset of 16-byte chunk cc (8 tokens) of head h's row in a P half
+// tile (64-byte rows, 64-byte swizzle: chunk cc of row h sits at
+// cc ^ ((h >> 1) & 3)).
+__device__ __forceinline__ uint32_t p_chunk(int h, int cc) {
+    return (uint32_t)(h * 64 + ((cc ^ ((h >> 1) & 3)) << 4));
+}
+
+// Scale head h's 32 bf16 values in one P half tile by f.
+__device__ __forceinline__ void scale_p_row(uint8_t *tile, int h, float f) {
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
-        uint4 *p = reinterpret_cast<uint4 *>(prow + (((4 * half + cc) ^ (h & 7)) << 4));
+        uint4 *p = reinterpret_cast<uint4 *>(tile + p_chunk(h, cc));
         uint4 v = *p;
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -296,8 +306,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             mbar_init(bar(ctl, B_PEMPTY + s), 1);
             mbar_init(bar(ctl, B_PEMPTY_PEER + s), 1);
             mbar_init(bar(ctl, B_SDONE + s), 4);
-            mbar_init(bar(ctl, B_PMSG + s), 128);
+            mbar_init(bar(ctl, B_PMSG + s), 1);
             mbar_init(bar(ctl, B_PREADY + s), 4);
+            mbar_init(bar(ctl, B_PREAD + s), 1);
         }
         mbar_init(bar(ctl, B_SFULL), 1);
         mbar_init(bar(ctl, B_QKP), 1);
@@ -436,7 +447,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         // Descriptor bases; every MMA below adds a byte offset (>> 4).
         const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
         const uint64_t d_k = smem_desc(s_k, 16, 1024, 2);
-        const uint64_t d_p = smem_desc(s_p, 16, 1024, 2);
+        const uint64_t d_p = smem_desc(s_p, 16, 512, 4);   // P halves: 64-byte swizzle
         const uint64_t d_vown = smem_desc(s_v + kVOwn, 4096, 1024, 2);
         const uint64_t d_vpeer = smem_desc(s_v + kVPeer, 4096, 1024, 2);
         constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
@@ -501,7 +512,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint64_t vb = (uint32_t)(ks >> 1) == rank ? d_vown : d_vpeer;
-                            mma_ss(tO, d_p + (uint64_t)((po + ks * 32) >> 4),
+                            mma_ss(tO, d_p + (uint64_t)((po + (ks >> 1) * kPHalf + (ks & 1) * 32) >> 4),
                                    vb + (uint64_t)((vo + (ks & 1) * 2048) >> 4), id_pv,
                                    (k == 0 && ks == 0) ? 0u : 1u);
                         }
@@ -635,12 +646,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     ok = false;
                     break;
                 }
-                // this half's P row and (max, row sum) -> this CTA's P slot; the merge
-                // warps copy them on into the peer's
+                // this half's P row and (max, row sum) -> this CTA's P slot; one bulk
+                // copy (issued by a merge warp) sends them on into the peer's
                 uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(pst + h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4)) =
+                    *reinterpret_cast<uint4 *>(pst + rank * kPHalf + p_chunk(h, cc)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
                 *reinterpret_cast<float2 *>(pst + kPMsg + rank * 1024 + h * 8) = make_float2(m_used, l_own);
                 fence_proxy_async_smem();
@@ -690,27 +701,36 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 const uint32_t gp = g + k, par = gp & 1, ps = gp % kPSlots, pu = gp / kPSlots;
                 if (!wait_warp(ctl, bar(ctl, B_SDONE + ps), pu & 1)) { ok = false; break; }
                 uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
-                {
-                    const uint32_t s_pst = s_p + ps * kPSlotBytes;
-                    const uint32_t r_pst = mapa(s_pst, peer);
-                    const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + ps), peer);
-                    mbar_arrive_expect_tx(bar(ctl, B_PMSG + ps), kMsgBytes);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint32_t off = h * 128 + (((4 * rank + cc) ^ (h & 7)) << 4);
-                        st_async_v4_b32(r_pst + off, *reinterpret_cast<const uint4 *>(pst + off), pmsg_peer);
+                const bool sender = warp == kMergeWarp0;
+                if (sender) {
+                    // one bulk copy of this CTA's P half and messages into the same
+                    // place in the peer's slot (the pair's link runs in the background)
+                    if (elect_one()) {
+                        const uint32_t s_pst = s_p + ps * kPSlotBytes;
+                        const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + ps), peer);
+                        mbar_arrive_expect_tx(bar(ctl, B_PMSG + ps), kMsgBytes);
+                        bulk_copy_s2c(mapa(s_pst + rank * kPHalf, peer), s_pst + rank * kPHalf, kPHalf, pmsg_peer);
+                        bulk_copy_s2c(mapa(s_pst + kPMsg + rank * 1024, peer), s_pst + kPMsg + rank * 1024,
+                                      1024, pmsg_peer);
+                        bulk_commit();
                     }
-                    const uint32_t moff = kPMsg + rank * 1024 + h * 8;
-                    const float2 mine = *reinterpret_cast<const float2 *>(pst + moff);
-                    st_async_v2_f32(r_pst + moff, mine.x, mine.y, pmsg_peer);
+                    __syncwarp();
                 }
                 if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) { ok = false; break; }
+                // this CTA's half may be rescaled in place only once the copy has read it
+                if (sender) {
+                    if (elect_one()) {
+                        bulk_wait_read_all();
+                        mbar_arrive(bar(ctl, B_PREAD + ps));
+                    }
+                    __syncwarp();
+                }
+                if (!wait_warp(ctl, bar(ctl, B_PREAD + ps), pu & 1)) { ok = false; break; }
                 const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPMsg + h * 8);
                 const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPMsg + 1024 + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
-                uint8_t *prow = pst + h * 128;
-                if (h0.x != NEG_INF && h0.x < nref) scale_p_half(prow, h, 0, fast_exp2(h0.x - nref));
-                if (h1.x != NEG_INF && h1.x < nref) scale_p_half(prow, h, 1, fast_exp2(h1.x - nref));
+                if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, fast_exp2(h0.x - nref));
+                if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPHalf, h, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
                 const bool need = k > 0 && nref > m_ref;
                 if (__any_sync(0xffffffffu, need)) {
@@ -863,6 +883,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         }
     }
 
+    // the bulk copies of warp 8 are complete before this CTA's shared memory goes away
+    if (warp == kMergeWarp0) {
+        if (elect_one()) bulk_wait_all();
+        __syncwarp();
+    }
     // teardown: both CTAs finish (no multicast or remote arrive in flight) before TMEM is freed
     tc_fence_before();
     __syncthreads();
