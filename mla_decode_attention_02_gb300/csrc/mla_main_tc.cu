@@ -75,9 +75,9 @@ constexpr int kClusterSize = 2;
 constexpr uint16_t kBoth = 0x3;
 constexpr int kHalfTok = 32;                      // tokens of a page per CTA
 constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-byte swizzle
-constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8
-constexpr uint32_t kVStageBytes = 8 * kBox;       // own, then peer tokens; output dims
-constexpr uint32_t kVOwn = 0, kVPeer = 4 * kBox;
+constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8 (one TMA box)
+constexpr uint32_t kVBlk = kPage * 128;           // 64 tokens x 64 dims, 128-byte swizzle
+constexpr uint32_t kVStageBytes = 4 * kVBlk;      // the page's tokens x output dims (one TMA box)
 constexpr uint32_t kPHalf = 128 * 64;             // one token half: 128 heads x 32 tokens, bf16,
                                                   // 64-byte swizzle; tile c = CTA c's tokens
 constexpr uint32_t kPMsg = 2 * kPHalf;            // (max, row sum) per head, 1 KB per CTA
@@ -113,16 +113,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 enum : uint32_t {
     B_Q_FULL = 0,                        // producer (+tx), softmax and merge warps (q in TMEM)
     B_Q_EMPTY = 1,                       // score issuers of both CTAs done with q
-    B_KFULL = 2,                         // + page parity: dim blocks 0-6 landed (+tx)
-    B_KFULLB = B_KFULL + 2,              // + page parity: blocks 7-8 landed (+tx)
-    B_KEMPTY = B_KFULLB + 2,             // + page parity: score MMAs done with the K stage
+    B_KFULL = 2,                         // + page parity: K stage landed (+tx)
+    B_KEMPTY = B_KFULL + 2,              // + page parity: score MMAs done with the K stage
     B_VFULL = B_KEMPTY + 2,              // + page parity: V stage landed (+tx)
     B_VEMPTY = B_VFULL + 2,              // + page parity: PV done with the V stage
     B_PEMPTY = B_VEMPTY + 2,             // + slot: this CTA's PV done with the P slot
     B_PEMPTY_PEER = B_PEMPTY + kPSlots,  // + slot: the peer's PV done with its P slot
     B_SFULL = B_PEMPTY_PEER + kPSlots,   // scores in TMEM
-    B_QKP = B_SFULL + 1,                 // the peer's scores done
-    B_SEMPTY = B_QKP + 1,                // scores read and the peer's seen, both CTAs
+    B_SEMPTY = B_SFULL + 1,              // scores read into registers
     B_SDONE = B_SEMPTY + 1,              // + slot: own P half written
     B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx)
     B_PREADY = B_PMSG + kPSlots,         // + slot: P tile final, PV may run
@@ -140,7 +138,11 @@ static_assert(B_COUNT * 8 <= 512, "barrier area");
 struct Params {
     CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
     CUtensorMap tm_q_rope;  // q_rope   as [rows*128][64],  box 64 x 128, SW128
-    CUtensorMap tm_kv;      // kv_cache as [pages][64][576], box 64 x 32 x 1, SW128
+    // kv_cache [pages][64][576] seen as (64 dims, 64 tokens, 9 dim blocks, pages) with
+    // the block stride 128 bytes: one box lands as stacked 128-byte-swizzled tiles
+    // [block][token][64 dims], the layout the MMAs read
+    CUtensorMap tm_k;       // box 64 x 32 x 9 x 1: a token half, all 576 dims
+    CUtensorMap tm_v;       // box 64 x 64 x 4 x 1: all 64 tokens, one CTA's 256 output dims
     const __nv_bfloat16 *q_latent;
     const int32_t *block_table;
     uint8_t *ws;
@@ -203,6 +205,47 @@ __device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
 __device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity,
                                           int scope = kCta) {
     return __all_sync(0xffffffffu, wait(c, b, parity, scope));
+}
+
+// Merge warp 8: wait for the peer's P half of page gp, and meanwhile send this
+// CTA's halves of pages sent .. gp + kPSlots - 1 whose softmax is done.  A send
+// arms this CTA's receive barrier of that page (its phase cannot complete
+// before) and bulk-copies the half and the messages into the peer's slot.
+__device__ bool send_and_wait(const Ctl &c, uint32_t s_p, uint32_t rank, uint32_t peer,
+                              uint32_t &sent, uint32_t total_pages, uint32_t gp) {
+    const uint32_t ps = gp % kPSlots, pu = gp / kPSlots;
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (sent < total_pages && sent <= gp + kPSlots - 1 &&
+            __all_sync(0xffffffffu, mbar_test_wait(bar(c, B_SDONE + sent % kPSlots), (sent / kPSlots) & 1))) {
+            if (elect_one()) {
+                const uint32_t s_pst = s_p + (sent % kPSlots) * kPSlotBytes;
+                const uint32_t pmsg = bar(c, B_PMSG + sent % kPSlots);
+                const uint32_t pmsg_peer = mapa(pmsg, peer);
+                mbar_arrive_expect_tx(pmsg, kMsgBytes);
+                bulk_copy_s2c(mapa(s_pst + rank * kPHalf, peer), s_pst + rank * kPHalf, kPHalf, pmsg_peer);
+                bulk_copy_s2c(mapa(s_pst + kPMsg + rank * 1024, peer), s_pst + kPMsg + rank * 1024, 1024,
+                              pmsg_peer);
+                bulk_commit();
+            }
+            __syncwarp();
+            ++sent;
+            continue;
+        }
+        if (sent > gp && __all_sync(0xffffffffu, mbar_test_wait_cluster(bar(c, B_PMSG + ps), pu & 1)))
+            return true;
+        if ((i & 255) == 255) {
+            if (__any_sync(0xffffffffu, *c.abort != 0)) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitLimitNs) {
+                if (elect_one()) fail(c);
+                __syncwarp();
+                return false;
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -296,7 +339,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_KFULL + p), 1);
-            mbar_init(bar(ctl, B_KFULLB + p), 1);
             mbar_init(bar(ctl, B_KEMPTY + p), 1);
             mbar_init(bar(ctl, B_VFULL + p), 1);
             mbar_init(bar(ctl, B_VEMPTY + p), 1);
@@ -311,8 +353,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             mbar_init(bar(ctl, B_PREAD + s), 1);
         }
         mbar_init(bar(ctl, B_SFULL), 1);
-        mbar_init(bar(ctl, B_QKP), 1);
-        mbar_init(bar(ctl, B_SEMPTY), 2 * 4);
+        mbar_init(bar(ctl, B_SEMPTY), 4);
         for (int r = 0; r < kRefLag; ++r) mbar_init(bar(ctl, B_RESDONE + r), 4);
         mbar_init(bar(ctl, B_PVLAST), 1);
         mbar_init(bar(ctl, B_OFREE), 4);
@@ -323,7 +364,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&P.tm_q_lat);
         prefetch_tmap(&P.tm_q_rope);
-        prefetch_tmap(&P.tm_kv);
+        prefetch_tmap(&P.tm_k);
+        prefetch_tmap(&P.tm_v);
     }
     if (warp == kQkWarp) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
@@ -354,7 +396,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     } else if (threadIdx.x == 0 && rank == 0) {
         atomicOr(&hdr->status, MLA_DEV_BAD_PLAN);
     }
-    const int tok_own = kHalfTok * (int)rank, tok_peer = kHalfTok * (int)peer;
+    const int tok_own = kHalfTok * (int)rank;
 
     if (warp == 0 || warp == kVWarp) {
         // ------------------------------------------------------------ TMA producers
@@ -385,16 +427,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             break;
                         }
                         if (lane == 0) {
-                            // blocks 0-6 (score MMAs with q in TMEM) and 7-8 complete
-                            // separate barriers, so those MMAs start before the rest lands
-                            const uint32_t fa = bar(ctl, B_KFULL + p), fb = bar(ctl, B_KFULLB + p);
-                            const uint32_t dst = s_k + p * kKStageBytes;
-                            mbar_arrive_expect_tx(fa, 7 * kBox);
-                            mbar_arrive_expect_tx(fb, 2 * kBox);
-#pragma unroll
-                            for (int blk = 0; blk < 9; ++blk)
-                                tma_load_3d(dst + blk * kBox, &P.tm_kv, 64 * blk, tok_own, page,
-                                            blk < 7 ? fa : fb);
+                            // one 36 KB box: an SM ingests a few large TMA copies much
+                            // faster than many 4 KB ones
+                            const uint32_t fa = bar(ctl, B_KFULL + p);
+                            mbar_arrive_expect_tx(fa, kKStageBytes);
+                            tma_load_4d(s_k + p * kKStageBytes, &P.tm_k, 0, tok_own, 0, page, fa);
                         }
                         if (k0 + kk == 0) {
                             // q dims 448-575, once the first page is on its way: both
@@ -417,8 +454,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         // warm L2 for a page beyond the ones in flight (each CTA warms
                         // its own token half, which the peer's V ring reads as well)
                         if (lane == 0 && k0 + kk + kPrefetch < n)
-                            for (int blk = 0; blk < 9; ++blk)
-                                tma_prefetch_3d(&P.tm_kv, 64 * blk, tok_own, page_ahead);
+                            tma_prefetch_4d(&P.tm_k, 0, tok_own, 0, page_ahead);
                     } else {
                         if (g >= 2 && !wait_warp(ctl, bar(ctl, B_VEMPTY + p), ((g >> 1) - 1) & 1)) {
                             ok = false;
@@ -426,14 +462,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         }
                         if (lane == 0) {
                             const uint32_t fv = bar(ctl, B_VFULL + p);
-                            const uint32_t dst = s_v + p * kVStageBytes;
                             mbar_arrive_expect_tx(fv, kVStageBytes);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int blk = 4 * (int)rank + j;
-                                tma_load_3d(dst + kVOwn + j * kBox, &P.tm_kv, 64 * blk, tok_own, page, fv);
-                                tma_load_3d(dst + kVPeer + j * kBox, &P.tm_kv, 64 * blk, tok_peer, page, fv);
-                            }
+                            tma_load_4d(s_v + p * kVStageBytes, &P.tm_v, 0, 0, 4 * (int)rank, page, fv);
                         }
                     }
                     __syncwarp();
@@ -448,8 +478,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const uint64_t d_qs = smem_desc(s_qs, 16, 1024, 2);
         const uint64_t d_k = smem_desc(s_k, 16, 1024, 2);
         const uint64_t d_p = smem_desc(s_p, 16, 512, 4);   // P halves: 64-byte swizzle
-        const uint64_t d_vown = smem_desc(s_v + kVOwn, 4096, 1024, 2);
-        const uint64_t d_vpeer = smem_desc(s_v + kVPeer, 4096, 1024, 2);
+        const uint64_t d_v = smem_desc(s_v, kVBlk, 1024, 2);  // MN-major: dim blocks kVBlk apart
         constexpr uint32_t id_qk = idesc_bf16(128, kHalfTok, 0, 0);
         constexpr uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
         const uint32_t tQ = tmem + kColQ, tO = tmem + kColO, tS = tmem + kColS;
@@ -467,7 +496,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     // has read the previous page's scores
                     const uint32_t ko = p * kKStageBytes;
                     if (!wait_warp(ctl, bar(ctl, B_KFULL + p), (g >> 1) & 1)) { ok = false; break; }
-                    if (g >= 1 && !wait_warp(ctl, bar(ctl, B_SEMPTY), (g - 1) & 1, kSignal)) {
+                    if (g >= 1 && !wait_warp(ctl, bar(ctl, B_SEMPTY), (g - 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -478,18 +507,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             mma_ts(tS, tQ + 8 * ks,
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, ks > 0 ? 1u : 0u);
-                    }
-                    __syncwarp();
-                    if (!wait_warp(ctl, bar(ctl, B_KFULLB + p), (g >> 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    if (elect_one()) {
 #pragma unroll
                         for (int ks = 28; ks < 36; ++ks)
                             mma_ss(tS, d_qs + (uint64_t)((((ks - 28) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, 1u);
                         mma_commit(bar(ctl, B_SFULL));
-                        mma_commit_mc(bar(ctl, B_QKP), peer_mask);
                         mma_commit(bar(ctl, B_KEMPTY + p));
                     }
                     __syncwarp();
@@ -510,12 +533,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t vb = (uint32_t)(ks >> 1) == rank ? d_vown : d_vpeer;
+                        for (int ks = 0; ks < 4; ++ks)
                             mma_ss(tO, d_p + (uint64_t)((po + (ks >> 1) * kPHalf + (ks & 1) * 32) >> 4),
-                                   vb + (uint64_t)((vo + (ks & 1) * 2048) >> 4), id_pv,
+                                   d_v + (uint64_t)((vo + ks * 2048) >> 4), id_pv,
                                    (k == 0 && ks == 0) ? 0u : 1u);
-                        }
                         mma_commit(bar(ctl, B_PVDONE + p));
                         mma_commit(bar(ctl, B_PEMPTY + ps));
                         mma_commit_mc(bar(ctl, B_PEMPTY_PEER + ps), peer_mask);
@@ -594,6 +615,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + kColS, r);
                 tmem_wait_ld();
+                // the scores are in registers: the next page's score MMAs may start
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_SEMPTY));
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
                 const int v_own = min(max(valid - tok_own, 0), kHalfTok);
@@ -613,17 +638,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                 }
                 const float lm = rmax * sc;
-                // The score buffer is released in both CTAs once the peer's scores of
-                // this page are seen: the peer's scores of page g + 1 (which complete
-                // the next phase of the QKP barrier) wait for it, so no phase is
-                // skipped.
-                if (!wait_warp(ctl, bar(ctl, B_QKP), g & 1, kSignal)) { ok = false; break; }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(ctl, B_SEMPTY));
-                    mbar_arrive_cluster_relaxed(mapa(bar(ctl, B_SEMPTY), peer));
-                }
                 // raise the max only when this half's page exceeds it by > 2^8
                 const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
                 const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : fast_exp2(m_prev - m_used));
@@ -669,6 +683,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
         bool ok = true;
+        // warp 8 sends this CTA's P halves: the next page to send and the unit's page count
+        uint32_t sent = 0, total_pages = 0;
+        for (int i = i_begin; i < i_end; ++i)
+            total_pages += (uint32_t)((items[i].kv_end - items[i].kv_begin + kPage - 1) / kPage);
         for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
             const int b = it.row / P.s_q;
@@ -701,29 +719,23 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 const uint32_t gp = g + k, par = gp & 1, ps = gp % kPSlots, pu = gp / kPSlots;
                 if (!wait_warp(ctl, bar(ctl, B_SDONE + ps), pu & 1)) { ok = false; break; }
                 uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
-                const bool sender = warp == kMergeWarp0;
-                if (sender) {
-                    // one bulk copy of this CTA's P half and messages into the same
-                    // place in the peer's slot (the pair's link runs in the background)
+                if (warp == kMergeWarp0) {
+                    // While the peer's half of this page is on its way, send this CTA's
+                    // halves of the pages the softmax has finished (up to kPSlots - 1
+                    // pages ahead), each as soon as it is ready.
+                    if (!send_and_wait(ctl, s_p, rank, peer, sent, total_pages, gp)) { ok = false; break; }
+                    // this CTA's half may be rescaled in place once the copy has read it
                     if (elect_one()) {
-                        const uint32_t s_pst = s_p + ps * kPSlotBytes;
-                        const uint32_t pmsg_peer = mapa(bar(ctl, B_PMSG + ps), peer);
-                        mbar_arrive_expect_tx(bar(ctl, B_PMSG + ps), kMsgBytes);
-                        bulk_copy_s2c(mapa(s_pst + rank * kPHalf, peer), s_pst + rank * kPHalf, kPHalf, pmsg_peer);
-                        bulk_copy_s2c(mapa(s_pst + kPMsg + rank * 1024, peer), s_pst + kPMsg + rank * 1024,
-                                      1024, pmsg_peer);
-                        bulk_commit();
-                    }
-                    __syncwarp();
-                }
-                if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) { ok = false; break; }
-                // this CTA's half may be rescaled in place only once the copy has read it
-                if (sender) {
-                    if (elect_one()) {
-                        bulk_wait_read_all();
+                        const uint32_t newer = sent - 1 - gp;   // copies issued after this page's
+                        if (newer == 0) bulk_wait_read<0>();
+                        else if (newer == 1) bulk_wait_read<1>();
+                        else bulk_wait_read<2>();
                         mbar_arrive(bar(ctl, B_PREAD + ps));
                     }
                     __syncwarp();
+                } else if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) {
+                    ok = false;
+                    break;
                 }
                 if (!wait_warp(ctl, bar(ctl, B_PREAD + ps), pu & 1)) { ok = false; break; }
                 const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPMsg + h * 8);
@@ -759,20 +771,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : fast_exp2(h1.x - nref));
                     l_run = h0.y * f0 + h1.y * f1;
                     if (valid_last < kPage) {
-                        // zero this CTA's latent rows of the masked tail (both token
-                        // halves) once they landed, so that 0 * garbage stays 0 in PV
+                        // zero this CTA's latent rows of the masked tail once they
+                        // landed, so that 0 * garbage stays 0 in PV
                         if (!wait_warp(ctl, bar(ctl, B_VFULL + par), (gp >> 1) & 1)) { ok = false; break; }
                         uint8_t *vst = smem + kOffV + par * kVStageBytes;
-                        const int v0 = min(max(valid_last - tok_own, 0), kHalfTok);
-                        const int v1 = min(max(valid_last - tok_peer, 0), kHalfTok);
-                        const int n0 = (kHalfTok - v0) * 8 * 4, n1 = (kHalfTok - v1) * 8 * 4;
-                        for (int idx = h; idx < n0 + n1; idx += 128) {
-                            const bool o = idx < n0;
-                            const int x = o ? idx : idx - n0;
-                            const int per_blk = (kHalfTok - (o ? v0 : v1)) * 8;
-                            const int blk = x / per_blk, rem = x % per_blk;
-                            const int tok = (o ? v0 : v1) + rem / 8;
-                            *reinterpret_cast<uint4 *>(vst + (o ? kVOwn : kVPeer) + blk * kBox + tok * 128 +
+                        const int per_blk = (kPage - valid_last) * 8;   // 16-byte chunks per dim block
+                        for (int idx = h; idx < 4 * per_blk; idx += 128) {
+                            const int blk = idx / per_blk, rem = idx % per_blk;
+                            *reinterpret_cast<uint4 *>(vst + blk * kVBlk + (valid_last + rem / 8) * 128 +
                                                        (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
                         }
                     }
@@ -918,7 +924,7 @@ bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
             const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -999,10 +1005,14 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
             return cudaErrorInvalidValue;
     }
     {
-        cuuint64_t dims[3] = {(cuuint64_t)kDrow, (cuuint64_t)kPage, (cuuint64_t)num_pages};
-        cuuint64_t strides[2] = {(cuuint64_t)kDrow * 2, (cuuint64_t)kDrow * 2 * kPage};
-        cuuint32_t box[3] = {64, (cuuint32_t)kHalfTok, 1};
-        if (!encode(&p.tm_kv, kv, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        // (dim within block, token, dim block, page); the block stride (128 bytes) is
+        // below the token stride, so a box lands block-major in shared memory
+        cuuint64_t dims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)(kDrow / 64), (cuuint64_t)num_pages};
+        cuuint64_t strides[3] = {(cuuint64_t)kDrow * 2, 128, (cuuint64_t)kDrow * 2 * kPage};
+        cuuint32_t box_k[4] = {64, (cuuint32_t)kHalfTok, (cuuint32_t)(kDrow / 64), 1};
+        cuuint32_t box_v[4] = {64, (cuuint32_t)kPage, 4, 1};
+        if (!encode(&p.tm_k, kv, 4, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&p.tm_v, kv, 4, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
     p.q_latent = static_cast<const __nv_bfloat16 *>(q_latent);
