@@ -29,13 +29,17 @@
 // CTA's 32 tokens of a page, all 576 dims, 36 KB) is freed by the score
 // MMAs; the V ring (the page's 64 tokens of this CTA's 256 output dims,
 // 32 KB; own tokens loaded a second time, from L2) and the P ring (the two
-// halves' P tiles and messages, 18 KB, three slots) are freed by PV.
+// halves' P tiles and messages, 18 KB, three slots) are freed by PV.  Each
+// K and V stage is one TMA box of a blocked view of the cache (one SM takes
+// in a few large TMA copies from L2 far faster than many 4 KB ones: about
+// 117 ns per copy plus 5 ns per KB, measured on this part).
 //
-// Measured on this part: one SM's shared memory streams about 250 GB/s;
-// the pair's distributed-shared-memory link about 27 GB/s per direction,
-// 0.34 us for a page's P half and messages (twice that while both SMs'
-// shared memory is busy), so it goes as one asynchronous bulk copy that no
-// warp waits on.
+// The P half goes to the peer as one asynchronous bulk copy (9 KB per
+// page), issued by merge warp 8 as soon as the softmax is done with the page:
+// while it waits for the peer's half of a page, it polls the softmax's
+// barriers of the next pages without blocking.  The copy runs on the same
+// engine as the page loads and arrives about 1 us after issue; the three P
+// slots cover that.
 //
 // TMEM (512 columns): O half [0,256), S [256,288), q [288,512).  Warp roles
 // per CTA: warp 0 loads the K ring and q, warp 2 the V ring; warp 1 issues
@@ -43,9 +47,10 @@
 // together and issues from one elected lane: about 15 ns per tcgen05.mma,
 // against 35 ns from a lane-0 branch); warps 4-7 (one per TMEM lane quarter,
 // one thread per head) load q into TMEM and compute P; warps 8-11 send P,
-// merge the two halves and run the epilogue.  Every wait is bounded: on
-// time-out the kernel records MLA_DEV_TIMEOUT and winds down instead of
-// hanging.
+// merge the two halves and run the epilogue.  The score buffer is released
+// right after the softmax's TMEM load, so the next page's score MMAs wait
+// only for that.  Every wait is bounded: on time-out the kernel records
+// MLA_DEV_TIMEOUT and winds down instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
