@@ -84,9 +84,11 @@ constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8 
 constexpr uint32_t kVBlk = kPage * 128;           // 64 tokens x 64 dims, 128-byte swizzle
 constexpr uint32_t kVStageBytes = 4 * kVBlk;      // the page's tokens x output dims (one TMA box)
 constexpr uint32_t kPHalf = 128 * 64;             // one token half: 128 heads x 32 tokens, bf16,
-                                                  // 64-byte swizzle; tile c = CTA c's tokens
-constexpr uint32_t kPMsg = 2 * kPHalf;            // (max, row sum) per head, 1 KB per CTA
-constexpr uint32_t kPSlotBytes = 2 * kPHalf + 2048;
+                                                  // 64-byte rows, 64-byte swizzle
+constexpr uint32_t kPPart = kPHalf + 1024;        // a CTA's part of a P slot: its half, then
+                                                  // (max, row sum) per head; one copy to the peer
+constexpr uint32_t kPSlotBytes = 2 * kPPart;
+static_assert(kPPart % 512 == 0, "64-byte-swizzle tiles start on 512-byte boundaries");
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
 constexpr int kQTDims = 448;                      // q dims 0-447 live in TMEM
 constexpr uint32_t kQSBytes = 2 * kQBlk;          // q dims 448-575 in shared memory
@@ -102,7 +104,7 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 &&
                   kKStageBytes % 1024 == 0 && kVStageBytes % 1024 == 0 && kPSlotBytes % 1024 == 0,
               "TMA/UMMA tile alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kMsgBytes = kPHalf + 1024;     // per page: P half tile + (max, row sum) per head
+constexpr uint32_t kMsgBytes = kPPart;            // per page: P half tile + (max, row sum) per head
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
@@ -228,9 +230,7 @@ __device__ bool send_and_wait(const Ctl &c, uint32_t s_p, uint32_t rank, uint32_
                 const uint32_t pmsg = bar(c, B_PMSG + sent % kPSlots);
                 const uint32_t pmsg_peer = mapa(pmsg, peer);
                 mbar_arrive_expect_tx(pmsg, kMsgBytes);
-                bulk_copy_s2c(mapa(s_pst + rank * kPHalf, peer), s_pst + rank * kPHalf, kPHalf, pmsg_peer);
-                bulk_copy_s2c(mapa(s_pst + kPMsg + rank * 1024, peer), s_pst + kPMsg + rank * 1024, 1024,
-                              pmsg_peer);
+                bulk_copy_s2c(mapa(s_pst + rank * kPPart, peer), s_pst + rank * kPPart, kPPart, pmsg_peer);
                 bulk_commit();
             }
             __syncwarp();
@@ -539,7 +539,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     if (elect_one()) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tO, d_p + (uint64_t)((po + (ks >> 1) * kPHalf + (ks & 1) * 32) >> 4),
+                            mma_ss(tO, d_p + (uint64_t)((po + (ks >> 1) * kPPart + (ks & 1) * 32) >> 4),
                                    d_v + (uint64_t)((vo + ks * 2048) >> 4), id_pv,
                                    (k == 0 && ks == 0) ? 0u : 1u);
                         mma_commit(bar(ctl, B_PVDONE + p));
@@ -670,9 +670,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(pst + rank * kPHalf + p_chunk(h, cc)) =
+                    *reinterpret_cast<uint4 *>(pst + rank * kPPart + p_chunk(h, cc)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                *reinterpret_cast<float2 *>(pst + kPMsg + rank * 1024 + h * 8) = make_float2(m_used, l_own);
+                *reinterpret_cast<float2 *>(pst + rank * kPPart + kPHalf + h * 8) = make_float2(m_used, l_own);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + ps));
@@ -743,11 +743,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     break;
                 }
                 if (!wait_warp(ctl, bar(ctl, B_PREAD + ps), pu & 1)) { ok = false; break; }
-                const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPMsg + h * 8);
-                const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPMsg + 1024 + h * 8);
+                const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPHalf + h * 8);
+                const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPPart + kPHalf + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
                 if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, fast_exp2(h0.x - nref));
-                if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPHalf, h, fast_exp2(h1.x - nref));
+                if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPPart, h, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
                 const bool need = k > 0 && nref > m_ref;
                 if (__any_sync(0xffffffffu, need)) {
