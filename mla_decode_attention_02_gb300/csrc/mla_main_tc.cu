@@ -118,7 +118,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,                        // producer (+tx), softmax and merge warps (q in TMEM)
+    B_Q_FULL = 0,                        // producer (+tx), softmax warps (q in TMEM)
     B_Q_EMPTY = 1,                       // score issuers of both CTAs done with q
     B_KFULL = 2,                         // + page parity: K stage landed (+tx)
     B_KEMPTY = B_KFULL + 2,              // + page parity: score MMAs done with the K stage
@@ -138,7 +138,8 @@ enum : uint32_t {
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
     B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
-    B_COUNT = B_DRAIN + 2,
+    B_QFULL0 = B_DRAIN + 2,              // first item: merge warps' part of q in TMEM
+    B_COUNT = B_QFULL0 + 1,
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 
@@ -340,7 +341,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(ctl, B_Q_FULL), 1 + 8);
+        mbar_init(bar(ctl, B_Q_FULL), 1 + 4);
+        mbar_init(bar(ctl, B_QFULL0), 4);
         mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_KFULL + p), 1);
@@ -454,6 +456,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                                     tma_load_2d_mc(s_qs, &P.tm_q_lat, kQTDims, y, fb, kBoth);
                                 else
                                     tma_load_2d_mc(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
+                                // warm L2 for the next item's q dims 0-447, which the
+                                // softmax warps load when this item's scores are done
+                                if (i + 1 < i_end)
+                                    for (int b = 0; b < kQTDims / 64; ++b)
+                                        tma_prefetch_2d(&P.tm_q_lat, 64 * b, items[i + 1].row * kHeads);
                             }
                         }
                         // warm L2 for a page beyond the ones in flight (each CTA warms
@@ -493,7 +500,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const WorkItem it = items[i];
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            if (qk && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+            if (qk && (!wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1) ||
+                       (ii == 0 && !wait_warp(ctl, bar(ctl, B_QFULL0), 0))))
+                break;
             for (int k = 0; k < n && ok; ++k, ++g) {
                 const uint32_t p = g & 1;
                 if (qk) {
@@ -586,13 +595,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q dims 0-255 of this head -> TMEM (the previous item's scores are
-            // done); the merge warps load dims 256-447
+            // q of this head -> TMEM: for the first item dims 0-255 (the merge
+            // warps load 256-447 meanwhile), for later items all of 0-447 once the
+            // previous item's scores are done (the rows are warm in L2; the merge
+            // warps are still busy with the previous item)
             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) break;
             {
                 const __nv_bfloat16 *qrow = P.q_latent + ((size_t)it.row * kHeads + h) * kDl;
                 load_q_chunks<2>(qrow, tQ, 0);
                 load_q_chunks<2>(qrow, tQ, 2);
+                if (ii > 0) load_q_chunks<3>(qrow, tQ, 4);
             }
             tc_fence_before();
             __syncwarp();
@@ -699,13 +711,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
-            // q dims 256-447 of this head -> TMEM (for later items this happens
-            // before the previous item's epilogue, so that their scores overlap it)
+            // q dims 256-447 of this head -> TMEM for the first item (the softmax
+            // warps load later items' q whole, while these warps finish the
+            // previous item)
             if (ii == 0) {
                 load_q_chunks<3>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tQ, 4);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
+                if (lane == 0) mbar_arrive(bar(ctl, B_QFULL0));
             }
             // every page of the item must lie in the pool
             bool bad = false;
@@ -798,13 +811,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
             g += n;
             if (!ok) break;
-            if (i + 1 < i_end) {
-                if (!wait_warp(ctl, bar(ctl, B_Q_EMPTY), ii & 1, kCluster)) break;
-                load_q_chunks<3>(P.q_latent + ((size_t)items[i + 1].row * kHeads + h) * kDl, tQ, 4);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_Q_FULL));
-            }
 
             // epilogue: wait for the last PV, normalise, store this CTA's half.  The
             // rows go through the last page's V stage (free now: its MMAs are done

@@ -222,6 +222,13 @@ __device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int32_t c0, in
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
