@@ -11,7 +11,7 @@ import workloads as W
 
 m = pytest.importorskip("mla_decode_attention_02_gb300")
 
-ITEM_COST = 4
+ITEM_COST = 10   # kItemCost of the planner (csrc/mla_internal.h)
 MIN_SPLIT = 8
 
 
