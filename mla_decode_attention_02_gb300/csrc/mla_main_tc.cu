@@ -138,8 +138,9 @@ enum : uint32_t {
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
     B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
-    B_QFULL0 = B_DRAIN + 2,              // first item: merge warps' part of q in TMEM
-    B_COUNT = B_QFULL0 + 1,
+    B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx, both CTAs' loads)
+    B_QCOPIED = B_QSTAGE + 1,            // item start: softmax warps moved the staged q to TMEM
+    B_COUNT = B_QCOPIED + 1,
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 
@@ -313,6 +314,37 @@ __device__ __forceinline__ void load_q_chunks(const __nv_bfloat16 *q_row, uint32
     tmem_wait_st();
 }
 
+// At an item's start q dims 0-255 (four 64-dim blocks, 128 heads each, 128-byte
+// swizzle) come in by TMA, each CTA loading half the blocks into both, through
+// buffers that are free then: blocks 0-1 in the K stage that the item's second
+// page will use (its first page loads into the other one meanwhile), 2-3 in
+// the shared-memory q tile (free once both CTAs' score MMAs of the previous
+// item are done).  Loading q through registers costs one L1 wavefront per head
+// row per instruction, so only dims 256-447 take that path, overlapped.
+constexpr int kQStaged = 4;
+__device__ __forceinline__ uint32_t q_stage_off(int b, uint32_t kstage) {
+    return b < 2 ? kOffK + kstage * kKStageBytes + b * kQBlk : kOffQS + (b - 2) * kQBlk;
+}
+static_assert(2 * kQBlk <= kKStageBytes && 2 * kQBlk <= kQSBytes && kQStaged * 64 < kQTDims, "q staging");
+
+// Head h's row of staged q block b -> TMEM columns [32 b, 32 b + 32): chunk c
+// (8 dims) of row h sits at c ^ (h & 7); eight consecutive heads read eight
+// different chunk positions, so the loads are free of bank conflicts.
+__device__ __forceinline__ void q_stage_to_tmem(const uint8_t *smem, int b, uint32_t kstage, int h,
+                                                uint32_t tq) {
+    const uint8_t *row = smem + q_stage_off(b, kstage) + h * 128;
+    uint32_t q[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(row + ((c ^ (h & 7)) << 4));
+        q[4 * c] = x.x;
+        q[4 * c + 1] = x.y;
+        q[4 * c + 2] = x.z;
+        q[4 * c + 3] = x.w;
+    }
+    tmem_st32(tq + b * 32, q);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 mla_main_tc_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
@@ -342,7 +374,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(bar(ctl, B_Q_FULL), 1 + 4);
-        mbar_init(bar(ctl, B_QFULL0), 4);
+        mbar_init(bar(ctl, B_QSTAGE), 1);
+        mbar_init(bar(ctl, B_QCOPIED), 4);
         mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_KFULL + p), 1);
@@ -429,6 +462,27 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const int page_ahead = __shfl_sync(0xffffffffu, ahead, kk);
                     const uint32_t p = g & 1;
                     if (kring) {
+                        if (k0 + kk == 0) {
+                            // Item start: both CTAs' score MMAs of the previous item are
+                            // done, so the K stage of this item's second page and the
+                            // shared-memory q tile are free.  Stage q dims 0-255 there
+                            // (see q_stage_off; each CTA loads half the blocks into both)
+                            // beside this page's K load; this item's q dims 448-575
+                            // follow (unicast: the peer may still be copying out of its
+                            // own tile) once the softmax warps moved the staged blocks
+                            // into TMEM.
+                            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
+                                ok = false;
+                                break;
+                            }
+                            if (lane == 0) {
+                                const uint32_t fq = bar(ctl, B_QSTAGE);
+                                mbar_arrive_expect_tx(fq, kQStaged * kQBlk);
+                                for (int b = (int)rank; b < kQStaged; b += 2)
+                                    tma_load_2d_mc(s_base + q_stage_off(b, p ^ 1), &P.tm_q_lat, 64 * b,
+                                                   it.row * kHeads, fq, kBoth);
+                            }
+                        }
                         if (g >= 2 && !wait_warp(ctl, bar(ctl, B_KEMPTY + p), ((g >> 1) - 1) & 1)) {
                             ok = false;
                             break;
@@ -441,10 +495,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             tma_load_4d(s_k + p * kKStageBytes, &P.tm_k, 0, tok_own, 0, page, fa);
                         }
                         if (k0 + kk == 0) {
-                            // q dims 448-575, once the first page is on its way: both
-                            // CTAs' copies must be free (last score MMAs of the previous
-                            // item done)
-                            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
+                            if (!wait_warp(ctl, bar(ctl, B_QCOPIED), ii & 1)) {
                                 ok = false;
                                 break;
                             }
@@ -452,15 +503,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                                 const uint32_t fb = bar(ctl, B_Q_FULL);
                                 mbar_arrive_expect_tx(fb, kQSBytes);
                                 const int y = it.row * kHeads;
-                                if (rank == 0)
-                                    tma_load_2d_mc(s_qs, &P.tm_q_lat, kQTDims, y, fb, kBoth);
-                                else
-                                    tma_load_2d_mc(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb, kBoth);
-                                // warm L2 for the next item's q dims 0-447, which the
-                                // softmax warps load when this item's scores are done
-                                if (i + 1 < i_end)
-                                    for (int b = 0; b < kQTDims / 64; ++b)
+                                tma_load_2d(s_qs, &P.tm_q_lat, kQTDims, y, fb);
+                                tma_load_2d(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb);
+                                // warm L2 for the next item's q
+                                if (i + 1 < i_end) {
+                                    for (int b = 0; b < kDl / 64; ++b)
                                         tma_prefetch_2d(&P.tm_q_lat, 64 * b, items[i + 1].row * kHeads);
+                                    tma_prefetch_2d(&P.tm_q_rope, 0, items[i + 1].row * kHeads);
+                                }
                             }
                         }
                         // warm L2 for a page beyond the ones in flight (each CTA warms
@@ -500,9 +550,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const WorkItem it = items[i];
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            if (qk && (!wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1) ||
-                       (ii == 0 && !wait_warp(ctl, bar(ctl, B_QFULL0), 0))))
-                break;
+            if (qk && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
             for (int k = 0; k < n && ok; ++k, ++g) {
                 const uint32_t p = g & 1;
                 if (qk) {
@@ -595,16 +643,35 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q of this head -> TMEM: for the first item dims 0-255 (the merge
-            // warps load 256-447 meanwhile), for later items all of 0-447 once the
-            // previous item's scores are done (the rows are warm in L2; the merge
-            // warps are still busy with the previous item)
-            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) break;
+            // q of this head -> TMEM: dims 0-255 from the staged blocks (the
+            // staging was issued after the previous item's score MMAs were done, into
+            // the K stage of the item's second page), dims 256-447 through registers
             {
-                const __nv_bfloat16 *qrow = P.q_latent + ((size_t)it.row * kHeads + h) * kDl;
-                load_q_chunks<2>(qrow, tQ, 0);
-                load_q_chunks<2>(qrow, tQ, 2);
-                if (ii > 0) load_q_chunks<3>(qrow, tQ, 4);
+                const uint4 *src = reinterpret_cast<const uint4 *>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl) +
+                                   kQStaged * 8;
+                uint4 x[24];
+#pragma unroll
+                for (int v = 0; v < 24; ++v) x[v] = src[v];
+                if (!wait_warp(ctl, bar(ctl, B_QSTAGE), ii & 1, kCluster)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int b = 0; b < kQStaged; ++b) q_stage_to_tmem(smem, b, (g & 1) ^ 1u, h, tQ);
+                // the staging buffers may be refilled: every read above has returned
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, B_QCOPIED));
+#pragma unroll
+                for (int c = 0; c < 3; ++c) {
+                    uint32_t q[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        q[4 * v] = x[c * 8 + v].x;
+                        q[4 * v + 1] = x[c * 8 + v].y;
+                        q[4 * v + 2] = x[c * 8 + v].z;
+                        q[4 * v + 3] = x[c * 8 + v].w;
+                    }
+                    tmem_st32(tQ + (kQStaged + c) * 32, q);
+                }
+                tmem_wait_st();
             }
             tc_fence_before();
             __syncwarp();
@@ -696,7 +763,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const int h = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_off + kColO;
-        const uint32_t tQ = tmem + lane_off + kColQ;
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
         bool ok = true;
@@ -711,15 +777,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
-            // q dims 256-447 of this head -> TMEM for the first item (the softmax
-            // warps load later items' q whole, while these warps finish the
-            // previous item)
-            if (ii == 0) {
-                load_q_chunks<3>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl, tQ, 4);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_QFULL0));
-            }
             // every page of the item must lie in the pool
             bool bad = false;
             for (int k0 = 0; k0 < n; k0 += 32) {
