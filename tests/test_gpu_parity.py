@@ -52,6 +52,23 @@ def test_split_rows_are_merged():
     assert_close(o, lse, o_ref, lse_ref, "split")
 
 
+@pytest.mark.parametrize("s_q,batch", [(1, 240), (2, 120)])
+def test_many_short_rows_packed(s_q, batch):
+    """Many short rows: units run several items back to back (item start: q staged by
+    TMA while the previous item drains), single-page items included; every element compared."""
+    rng = np.random.default_rng(50 + s_q)
+    lens = [int(x) for x in rng.integers(s_q, 300, size=batch)]
+    lens[:4] = [s_q, 64, 65, 299]
+    w = W.custom(lens, s_q=s_q, seed=51 + s_q)
+    inp = W.make_inputs(w, poison=True, extra_pages=4)
+    d = to_device(inp)
+    p = mla.plan(d["seq_lens"], s_q=s_q, max_pages_per_seq=d["block_table"].shape[1])
+    r = mla.parse_plan(mla.plan_device_bytes(p), w.batch, s_q, mla.num_units())
+    items_per_unit = np.diff(r["unit_begin"])
+    assert items_per_unit.max() >= 3
+    _parity_full(w, poison=True, extra_pages=4)
+
+
 def test_mtp_small():
     _parity_full(W.custom([2, 64, 65, 1024, 2049, 8192], s_q=2, seed=41), poison=True)
 
