@@ -6,11 +6,14 @@
 //   M = max_i lse_i,  w_i = exp(lse_i - M),
 //   o = sum_i w_i o_i / sum_i w_i  (-> bf16),  lse = M + ln sum_i w_i.
 //
-// One warp per (row, head) task, warps striding over all tasks (a fixed,
-// small grid: most rows of most schedules are not split and cost one load);
-// each lane owns 16 of the 512 output values as four float4 columns, so
-// every partial row is read fully coalesced.  The pieces are summed in index
-// order: the result does not depend on timing.
+// Rows of up to kWarpParts pieces: one warp per (row, head) task, warps
+// striding over all tasks (most rows of most schedules are not split and cost
+// one load).  Rows of more pieces (one long request spread over many SM
+// pairs): one CTA per (row, head) task, its warps sharing the pieces, so that
+// the reads of a single long request are spread over many SMs.  Each lane owns
+// 16 of the 512 output values as four float4 columns, so every partial row is
+// read fully coalesced.  The pieces are summed in a fixed order: the result
+// does not depend on timing.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,9 +26,96 @@ namespace {
 constexpr int kCombineWarps = 8;
 constexpr int kCombineGrid = 1024;  // CTAs; warps stride over (row, head) tasks
 
+constexpr int kWarpParts = 8;      // rows with more parts are merged by a whole CTA per head
+
+// o = acc / W -> bf16 (lane owns four float4 columns of the 512), lse = M + ln W.
+__device__ __forceinline__ void store_row(__nv_bfloat16 *orow, float *lse, const float4 (&acc)[4], float W,
+                                          float M, int lane) {
+    const float inv = 1.f / W;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(orow)[k * 32 + lane] = packed;
+    }
+    if (lane == 0) *lse = M + logf(W);
+}
+
+// One (row, head) task of a row of many parts, by the whole CTA: warp w sums
+// parts w, w + 8, ...; the warps' sums are added in warp order (the result
+// does not depend on timing).
+__device__ __forceinline__ void merge_task_cta(int32_t r, int32_t h, int32_t n, const int32_t *row_part0,
+                                               const float *lse_part, const float *o_part,
+                                               __nv_bfloat16 *o_latent, float *lse_out, int lane, int warp,
+                                               float4 (&red)[kCombineWarps][4][32], float (&red_w)[kCombineWarps],
+                                               float (&red_m)[kCombineWarps]) {
+    __nv_bfloat16 *orow = o_latent + ((size_t)r * kHeads + h) * kDl;
+    const int32_t part0 = row_part0[r];
+    // M = max over all parts (each warp over its parts, then across warps)
+    float m = -INFINITY;
+    for (int32_t i = warp * 32 + lane; i < n; i += kCombineWarps * 32)
+        m = fmaxf(m, lse_part[(size_t)(part0 + i) * kHeads + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red_m[warp] = m;
+    __syncthreads();
+    float M = red_m[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
+
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    for (int32_t i = warp; i < n; i += kCombineWarps) {
+        const size_t slot = (size_t)(part0 + i) * kHeads + h;
+        const float w = expf(lse_part[slot] - M);
+        W += w;
+        const float4 *src = reinterpret_cast<const float4 *>(o_part + slot * kDl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 v = src[k * 32 + lane];
+            acc[k].x += w * v.x;
+            acc[k].y += w * v.y;
+            acc[k].z += w * v.z;
+            acc[k].w += w * v.w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) red[warp][k][lane] = acc[k];
+    if (lane == 0) red_w[warp] = W;
+    __syncthreads();
+    // warp 0 sums the warps' partial sums in warp order (the result does not
+    // depend on timing) and writes the row
+    if (warp == 0) {
+        float Wt = 0.f;
+        float4 t[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < kCombineWarps; ++w) {
+            Wt += red_w[w];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = red[w][k][lane];
+                t[k].x += v.x;
+                t[k].y += v.y;
+                t[k].z += v.z;
+                t[k].w += v.w;
+            }
+        }
+        store_row(orow, lse_out + (size_t)r * kHeads + h, t, Wt, M, lane);
+    }
+    __syncthreads();   // red / red_m are reused by the next task
+}
+
 __global__ void __launch_bounds__(32 * kCombineWarps)
 mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o_latent,
                    float *__restrict__ lse_out, int32_t batch, int32_t s_q, int32_t num_units) {
+    __shared__ float4 red[kCombineWarps][4][32];   // per warp: its lanes' 16 partial sums
+    __shared__ float red_w[kCombineWarps], red_m[kCombineWarps];
     // launched as a programmatic dependent of the main kernel
     ptx::pdl_wait_prior();
     // nothing to merge when no row was split and every row was valid: the main
@@ -33,19 +123,21 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(ws);
     if (hdr->num_parts == 0 && (hdr->status & MLA_DEV_BAD_SEQ_LEN) == 0) return;
     const PlanLayout L = plan_layout(batch, s_q, num_units);
-    const int32_t lane = threadIdx.x & 31;
+    const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t tasks = (int64_t)L.num_rows * kHeads;
-    const int64_t stride = (int64_t)gridDim.x * kCombineWarps;
     const int32_t *row_nparts = reinterpret_cast<const int32_t *>(ws + L.row_nparts);
     const int32_t *row_part0 = reinterpret_cast<const int32_t *>(ws + L.row_part0);
     const float *lse_part = reinterpret_cast<const float *>(ws + L.lse_part);
     const float *o_part = reinterpret_cast<const float *>(ws + L.o_part);
-    for (int64_t task = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5); task < tasks;
-         task += stride) {
+
+    // Rows of a few parts: one warp per (row, head) task, warps strided over
+    // the tasks; the parts are summed in index order.
+    for (int64_t task = (int64_t)blockIdx.x * kCombineWarps + warp; task < tasks;
+         task += (int64_t)gridDim.x * kCombineWarps) {
         const int32_t r = (int32_t)(task / kHeads);
         const int32_t h = (int32_t)(task % kHeads);
         const int32_t n = row_nparts[r];
-        if (n == 1) continue;  // the main kernel wrote this row directly
+        if (n == 1 || n > kWarpParts) continue;  // written by the main kernel / merged below
         __nv_bfloat16 *orow = o_latent + ((size_t)r * kHeads + h) * kDl;
         if (n == 0) {          // invalid row (bad seq_len): NaN, flagged in the status word
             const __nv_bfloat16 nan = __float2bfloat16(__int_as_float(0x7fc00000));
@@ -55,11 +147,9 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
         }
         const int32_t part0 = row_part0[r];
         float M = -INFINITY;
-        for (int32_t i = lane; i < n; i += 32)
-            M = fmaxf(M, lse_part[(size_t)(part0 + i) * kHeads + h]);
+        for (int32_t i = lane; i < n; i += 32) M = fmaxf(M, lse_part[(size_t)(part0 + i) * kHeads + h]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
         float4 acc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -78,17 +168,20 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
                 acc[k].w += w * v.w;
             }
         }
-        const float inv = 1.f / W;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t *>(&lo);
-            packed.y = *reinterpret_cast<uint32_t *>(&hi);
-            reinterpret_cast<uint2 *>(orow)[k * 32 + lane] = packed;
-        }
-        if (lane == 0) lse_out[(size_t)r * kHeads + h] = M + logf(W);
+        store_row(orow, lse_out + (size_t)r * kHeads + h, acc, W, M, lane);
+    }
+
+    // Rows of many parts (one long request over many SM pairs): one (row,
+    // head) task per CTA, tasks strided over the grid; the CTA's warps share
+    // the parts (merge_task_cta).  Skipped at once when no row has that many.
+    int big = 0;
+    for (int32_t r = threadIdx.x; r < L.num_rows; r += blockDim.x) big |= row_nparts[r] > kWarpParts;
+    if (!__syncthreads_or(big)) return;
+    for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
+        const int32_t n = row_nparts[task / kHeads];
+        if (n <= kWarpParts) continue;   // CTA-uniform: every thread skips together
+        merge_task_cta((int32_t)(task / kHeads), (int32_t)(task % kHeads), n, row_part0, lse_part, o_part,
+                       o_latent, lse_out, lane, warp, red, red_w, red_m);
     }
 }
 
@@ -97,8 +190,7 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
 cudaError_t launch_combine(const void *ws, void *o_latent, float *lse, int32_t batch, int32_t s_q,
                            int32_t num_units, cudaStream_t stream) {
     const int64_t tasks = (int64_t)batch * s_q * kHeads;
-    const int64_t need = (tasks + kCombineWarps - 1) / kCombineWarps;
-    const int grid = (int)(need < kCombineGrid ? need : kCombineGrid);
+    const int grid = (int)(tasks < kCombineGrid ? tasks : kCombineGrid);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(32 * kCombineWarps);
