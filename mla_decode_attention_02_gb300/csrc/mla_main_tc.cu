@@ -178,8 +178,8 @@ __device__ __forceinline__ void fail(const Ctl &c) {
 }
 
 // How a wait acquires: CTA scope; cluster scope, for phases that the peer
-// CTA completes with data (st.async, TMA multicast, its MMAs' commits); or
-// not at all, for pure progress signals from the peer.
+// CTA completes with data (its bulk copies, TMA multicast, its MMAs'
+// commits); or not at all, for pure progress signals from the peer.
 enum Scope : int { kCta = 0, kCluster = 1, kSignal = 2 };
 
 __device__ __forceinline__ bool try_wait(uint32_t b, uint32_t parity, int scope) {
@@ -288,30 +288,6 @@ __device__ __forceinline__ void scale_p_row(uint8_t *tile, int h, float f) {
         }
         *p = make_uint4(w[0], w[1], w[2], w[3]);
     }
-}
-
-// q dims [64 c0, 64 (c0 + N)) of one head -> TMEM columns [32 c0, 32 (c0 + N)).
-// All loads are in flight before the first store, so N chunks cost one memory
-// round trip.
-template <int N>
-__device__ __forceinline__ void load_q_chunks(const __nv_bfloat16 *q_row, uint32_t tq, int c0) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(q_row) + c0 * 8;
-    uint4 x[8 * N];
-#pragma unroll
-    for (int v = 0; v < 8 * N; ++v) x[v] = src[v];
-#pragma unroll
-    for (int c = 0; c < N; ++c) {
-        uint32_t q[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            q[4 * v] = x[c * 8 + v].x;
-            q[4 * v + 1] = x[c * 8 + v].y;
-            q[4 * v + 2] = x[c * 8 + v].z;
-            q[4 * v + 3] = x[c * 8 + v].w;
-        }
-        tmem_st32(tq + (c0 + c) * 32, q);
-    }
-    tmem_wait_st();
 }
 
 // At an item's start q dims 0-255 (four 64-dim blocks, 128 heads each, 128-byte

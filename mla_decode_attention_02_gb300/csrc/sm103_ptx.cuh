@@ -74,19 +74,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-                 : "memory");
-}
-
-// Arrive on another CTA's mbarrier with no memory ordering: for signals that
-// carry no data (the release form costs ~0.5-1 us on this part).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -167,15 +154,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
-                                            int32_t c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
                                             int32_t c2, int32_t c3, uint32_t bar) {
     asm volatile(
@@ -187,16 +165,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int3
 
 // Same load, written to the same shared-memory offset of every CTA in cta_mask;
 // each destination CTA's mbarrier (same offset) receives the complete_tx.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, int32_t c0,
-                                               int32_t c1, int32_t c2, uint32_t bar,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, int32_t c0,
                                                int32_t c1, uint32_t bar, uint16_t cta_mask) {
     asm volatile(
@@ -207,13 +175,6 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, i
 }
 
 // Bring a tensor tile into L2 ahead of its load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int32_t c0, int32_t c1, int32_t c2,
                                                 int32_t c3) {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global [%0, {%1, %2, %3, %4}];" ::"l"(
@@ -232,34 +193,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, in
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 16-byte store into another CTA's shared memory that completes `bytes` of the
-// transaction count of that CTA's mbarrier (both addresses from mapa).
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
-                                            float d, uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
-            "r"(remote_addr),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void st_async_v4_b32(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-            "r"(remote_addr),
-        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void st_async_v2_f32(uint32_t remote_addr, float a, float b,
-                                                uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-            remote_addr),
-        "f"(a), "f"(b), "r"(remote_bar)
-        : "memory");
 }
 
 // One lane of a fully active warp (the same lane every time): issuing tcgen05
@@ -287,11 +220,6 @@ __device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src
 
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until every bulk copy this thread committed has read its source.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Wait until all but the N most recent bulk-copy groups of this thread have read their sources.
