@@ -31,11 +31,13 @@
 namespace mla {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;   // one CTA; fewer threads make its block-wide barriers cheaper
+static_assert(kPlanThreads % 32 == 0 && kPlanThreads <= 1024, "planner block");
 constexpr size_t kMaxPlanSmem = 200 * 1024;  // per-row working set of the planner kernel
 
 
-// Inclusive block-wide sum of one int64 per thread (1024 threads).
+// Inclusive block-wide sum of one int64 per thread (kPlanThreads threads, at
+// most 32 warps).
 __device__ int64_t block_inclusive_sum(int64_t v, int64_t *warp_sums) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -46,7 +48,7 @@ __device__ int64_t block_inclusive_sum(int64_t v, int64_t *warp_sums) {
     if (lane == 31) warp_sums[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        int64_t w = warp_sums[lane];
+        int64_t w = lane < kPlanThreads / 32 ? warp_sums[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int64_t n = __shfl_up_sync(0xffffffffu, w, o);
