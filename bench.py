@@ -67,6 +67,27 @@ def _dist():
 _CUDART = None
 
 
+def reduce_over_ranks(values, op: str, world: int, device=None) -> list:
+    """Fold per-rank numbers over all ranks ("max" or "min"); the identity on one rank.
+
+    The timed region counts at its slowest rank (max); the adaptive step count
+    is the smallest any rank chose (min), so every rank runs the same steps.
+    NCCL ranks pass their CUDA device; gloo ranks (the CPU tests) pass none.
+    """
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.MIN)
+    return t.tolist()
+
+
+def whole_job_tbs(world: int, cache_bytes_per_rank: float, step_ms: float) -> float:
+    """Whole-job cache TB/s: every rank runs the full workload (weak scaling)."""
+    return world * cache_bytes_per_rank / (step_ms * 1e-3) / 1e12
+
+
 def _cudart():
     import ctypes
     global _CUDART
@@ -335,10 +356,7 @@ def run_native(args, rank, world, local):
             torch.cuda.synchronize()
             per = e0.elapsed_time(e1) / 5 / 1e3
         steps = int(min(4000 if not args.no_graph else 20000, max(20, 3.0 / max(per, 1e-6))))
-        if world > 1:
-            t = torch.tensor([steps], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MIN)
-            steps = int(t.item())
+        steps = int(reduce_over_ranks([steps], "min", world, dev)[0])
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     ev_s = [mk() for _ in range(steps)]
@@ -403,14 +421,12 @@ def run_native(args, rank, world, local):
     main_ms = statistics.mean(_event_ms(ev_k[k][0], ev_k[k][1]) for k in range(steps))
     comb_ms = statistics.mean(_event_ms(ev_k[k][1], ev_k[k][2]) for k in range(steps))
     plan_ms = statistics.mean(_event_ms(ev_s[k], ev_k[k][0]) for k in range(steps))
-    if world > 1:
-        t = torch.tensor([step_ms, main_ms, comb_ms, plan_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, main_ms, comb_ms, plan_ms = t.tolist()
+    step_ms, main_ms, comb_ms, plan_ms = reduce_over_ranks([step_ms, main_ms, comb_ms, plan_ms], "max",
+                                                           world, dev)
 
     cache_b = W.cache_bytes(w.seq_lens)
     fl = W.flops(w.seq_lens, S)
-    value = world * cache_b / (step_ms * 1e-3) / 1e12
+    value = whole_job_tbs(world, cache_b, step_ms)
 
     # end to end through the public API: pinned host inputs -> device, step, result -> host
     e2e = None
@@ -445,11 +461,8 @@ def run_native(args, rank, world, local):
             ee[k].record(stream)
         torch.cuda.synchronize()
         e2e_ms = statistics.mean(es[k].elapsed_time(ee[k]) for k in range(k_e2e))
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = t.item()
-        e2e = {"value": world * cache_b / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+        e2e_ms = reduce_over_ranks([e2e_ms], "max", world, dev)[0]
+        e2e = {"value": whole_job_tbs(world, cache_b, e2e_ms), "unit": "TB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": k_e2e,
                "note": "per-step inputs (q_latent, q_rope, block_table, seq_lens) copied from "
