@@ -69,6 +69,27 @@ def test_many_short_rows_packed(s_q, batch):
     _parity_full(w, poison=True, extra_pages=4)
 
 
+@pytest.mark.parametrize("s_q", [1, 2])
+def test_rising_scores_rescale(s_q):
+    """Scores that keep rising along each row: each page's k_rope is scaled up with its page
+    index (and q_rope by 3), so the running max grows by more than 2^8 again and again and
+    the kernel rescales O and the lower P half on many pages.  V (c_kv) is left at N(0, 1),
+    so the tolerance still measures the attention, not bf16 rounding of large outputs."""
+    lens = [700, 1500, 3000, 64, 130, 2049]
+    w = W.custom(lens, s_q=s_q, seed=60 + s_q)
+    inp = W.make_inputs(w)
+    inp["q_rope"] = (inp["q_rope"].float() * 3).to(torch.bfloat16)
+    kv = inp["kv_cache"].float()
+    bt = inp["block_table"]
+    for b, L in enumerate(lens):
+        for pi in range((L + 63) // 64):
+            kv[int(bt[b, pi]), :, W.D_LATENT:] *= 1.0 + pi / 4.0
+    inp["kv_cache"] = kv.to(torch.bfloat16)
+    o, lse, _ = run_gpu(inp)
+    o_ref, lse_ref = oracle_full(inp)
+    assert_close(o, lse, o_ref, lse_ref, "rising scores")
+
+
 def test_mtp_small():
     _parity_full(W.custom([2, 64, 65, 1024, 2049, 8192], s_q=2, seed=41), poison=True)
 
