@@ -16,6 +16,10 @@ TPOT-jitter troubleshooting post.
 Pins (tests that tie it to something other than itself) live in
 ``tests/test_oracle_pins.py``: the unabsorbed multi-head form, a dense fp64
 library softmax on tiny inputs, closed forms, and invariants.
+
+``oracle.prolog`` (numpy, fp64) holds the step before attention: the
+absorbed query projection, RoPE, RMSNorm of the new latent and the append
+into the paged cache; its pins are in ``tests/test_prolog_pins.py``.
 """
 
 from __future__ import annotations
