@@ -8,6 +8,7 @@ workload is the 4K-uniform decode batch (B=64, s_q=1, 128 heads, every
 seq_len 4096); ``--workload`` picks another for manual runs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+    python bench.py --stage prolog [--workload W]     # the step before attention, alone
 
 Prints one JSON line.  ``value`` is KV-cache TB/s (algorithmic bytes: every
 cached row once, 1152 B per key) over all ranks; TFLOPS, microseconds per
@@ -36,6 +37,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode KV-cache TB/s, TFLOPS and % of GB300 roofline; µs per decode step"
+PROLOG_METRIC = "MLA prolog (absorbed q, RoPE, RMSNorm, paged append) algorithmic HBM GB/s; µs per launch"
 NOMINAL_HBM_TBS = 8.0
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -49,6 +51,8 @@ def _args():
                     help="timed steps (default: enough for ~3 s of timed work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--stage", choices=["decode", "prolog"], default="decode",
+                    help="decode: the attention step (default); prolog: the step before it alone")
     ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -517,11 +521,131 @@ def run_native(args, rank, world, local):
     return 0
 
 
+def run_prolog(args, rank, world, local):
+    """--stage prolog: the prolog launch alone (absorbed q, RoPE, RMSNorm, cache append).
+
+    The workload's new tokens (batch x s_q) with a pool holding just their pages;
+    L2 is flushed (256 MiB written) before every timed launch, and each launch
+    is bracketed by CUDA events on its stream.  value = algorithmic bytes per
+    launch (every input read once, every output written once) / launch time.
+    """
+    import torch
+    import mla_decode_attention_02_gb300 as mla
+
+    if world > 1:
+        raise SystemExit("--stage prolog runs on one GPU")
+    w = W.workload(args.workload)
+    B, S = w.batch, w.s_q
+    if args.impl == "reference":
+        from oracle import prolog as OP
+        t = W.prolog_tensors(B, S, w.seed)
+        c = W.sparse_cache(w.seq_lens, S, w.seed)
+        times = []
+        for _ in range(max(1, args.steps or 3)):
+            t0 = time.perf_counter()
+            OP.prolog(t["q_nope"], t["q_pe"], t["kv_latent"], t["k_pe"], t["w_uk"],
+                      t["kv_norm_weight"], c["kv_cache"], c["block_table"], c["seq_lens"])
+            times.append(time.perf_counter() - t0)
+        sec = statistics.median(times)
+        nbytes = W.prolog_bytes(B, S)
+        print(json.dumps({"metric": PROLOG_METRIC, "stage": "prolog", "impl": "reference",
+                          "value": nbytes / sec / 1e9, "unit": "GB/s", "us_per_launch": sec * 1e6,
+                          "higher_is_better": True, "n_gpus": 1, "dtype": "f64",
+                          "config": {"workload": w.name, "tokens": B * S}}), flush=True)
+        return 0
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t = {k: v.to(dev) for k, v in W.prolog_tensors(B, S, w.seed).items()}
+    c_cpu = W.sparse_cache(w.seq_lens, S, w.seed)
+    c = {k: v.to(dev) for k, v in c_cpu.items()}
+    q_lat = torch.empty((B, S, W.NUM_HEADS, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    q_rope = torch.empty((B, S, W.NUM_HEADS, W.D_ROPE), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    table = mla.rope_table(W.ROPE_BASE, dev)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        mla.prolog(t["q_nope"], t["q_pe"], t["kv_latent"], t["k_pe"], t["w_uk"], t["kv_norm_weight"],
+                   c["kv_cache"], c["block_table"], c["seq_lens"], table=table, q_latent=q_lat,
+                   q_rope=q_rope, status=status)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        launch()
+    torch.cuda.synchronize()
+    steps = args.steps or 500
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+
+    def timed(external: bool):
+        cur = torch.cuda.current_stream()
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            _record(ev[k][0], cur, external)
+            launch()
+            _record(ev[k][1], cur, external)
+
+    # the K launches are one CUDA graph, so the GPU never waits for the host between them
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            timed(external=True)
+        torch.cuda.synchronize()
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.5)
+    t_start = time.time()
+    if graph is not None:
+        graph.replay()
+    else:
+        timed(external=False)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    clocks = sampler.summary(t_start, t_end)
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} in the prolog")
+    us = [_event_ms(e0, e1) * 1e3 for e0, e1 in ev]
+    us_mean = statistics.mean(us)
+    nbytes = W.prolog_bytes(B, S)
+    fl = W.prolog_flops(B, S)
+    peaks, peak_src = _peaks()
+    gbs = nbytes / (us_mean * 1e-6) / 1e9
+    line = {"metric": PROLOG_METRIC, "stage": "prolog", "value": gbs, "unit": "GB/s",
+            "us_per_launch": us_mean, "us_median": statistics.median(us), "us_min": min(us),
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "s_q": S, "tokens": B * S,
+                       "l2": "flushed (256 MiB written) before every launch"},
+            "tflops": fl / (us_mean * 1e-6) / 1e12,
+            "roofline": {"kernel": "mla_prolog", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": fl},
+            "gpu_launches": steps, "clocks": clocks, "launch": "eager" if args.no_graph else "cuda_graph",
+            "device": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = _args()
     rank, world, local = _dist()
     if world != args.gpus and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.stage == "prolog":
+        return run_prolog(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_native(args, rank, world, local)

@@ -7,16 +7,22 @@ ctypes binding with the same names:
     p = plan(seq_lens, s_q=1, max_pages_per_seq=maxp)       # mla_decode_plan
     o_latent, lse = decode(p, q_latent, q_rope, kv_cache, block_table)   # mla_decode
     status = check(p)                                         # mla_decode_check
+
+The step before attention (``include/mla_prolog.h``) produces q_latent and
+q_rope and appends the step's rows to the cache:
+
+    q_latent, q_rope, st = prolog(q_nope, q_pe, kv_latent, k_pe, w_uk, gamma,
+                                  kv_cache, block_table, seq_lens)   # mla_prolog
 """
 
-from ._binding import (DEFAULT_SCALE, D_LATENT, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
+from ._binding import (DEFAULT_ROPE_BASE, DEFAULT_RMS_EPS, DEFAULT_SCALE, D_LATENT, D_NOPE, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
                        MLA_DEV_BAD_PAGE, MLA_DEV_BAD_PLAN, MLA_DEV_BAD_SEQ_LEN, MLA_DEV_TIMEOUT,
                        MLAError, NOALLOC_SCRATCH_BYTES, Plan, check, decode, decode_noalloc,
-                       load_library, num_units, parse_plan, plan,
+                       load_library, num_units, parse_plan, plan, prolog, rope_table,
                        plan_device_bytes, plan_host, plan_layout, workspace_size)
 
-__all__ = ["DEFAULT_SCALE", "D_LATENT", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
+__all__ = ["DEFAULT_ROPE_BASE", "DEFAULT_RMS_EPS", "DEFAULT_SCALE", "D_LATENT", "D_NOPE", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
            "MLA_DEV_BAD_PAGE", "MLA_DEV_BAD_PLAN", "MLA_DEV_BAD_SEQ_LEN", "MLA_DEV_TIMEOUT",
            "MLAError", "NOALLOC_SCRATCH_BYTES", "Plan", "check", "decode", "decode_noalloc",
            "load_library", "num_units", "parse_plan",
-           "plan", "plan_device_bytes", "plan_host", "plan_layout", "workspace_size"]
+           "plan", "plan_device_bytes", "prolog", "rope_table", "plan_host", "plan_layout", "workspace_size"]

@@ -62,6 +62,9 @@ _SIGS = {
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mla_decode_plan_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
     "mla_decode_plan_host": (ctypes.c_int, [_P, _vp, ctypes.c_int32, _vp, ctypes.c_size_t]),
+    "mla_prolog": (ctypes.c_int, [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                  _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mla_prolog_rope_table": (ctypes.c_int, [ctypes.c_double, _vp, _vp]),
 }
 
 
@@ -244,6 +247,83 @@ def decode_noalloc(q_latent, q_rope, kv_cache, block_table, seq_lens, *, s_q: in
             kv_cache.shape[0], block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
             out.data_ptr(), lse.data_ptr(), _stream_handle(stream)), "mla_decode_noalloc")
     return out, lse
+
+
+D_NOPE = 128
+DEFAULT_ROPE_BASE = 10000.0
+DEFAULT_RMS_EPS = 1e-6
+
+
+ROPE_TABLE_FLOATS = 64
+_rope_tables = {}
+
+
+def rope_table(rope_base: float = DEFAULT_ROPE_BASE, device=None, stream=None):
+    """The rotary table of ``mla_prolog_rope_table`` (float32 [64] on the device), built on the GPU."""
+    import torch
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        table = torch.empty(ROPE_TABLE_FLOATS, dtype=torch.float32, device=dev)
+        _check(load_library().mla_prolog_rope_table(float(rope_base), table.data_ptr(),
+                                                    _stream_handle(stream)), "mla_prolog_rope_table")
+    return table
+
+
+def prolog(q_nope, q_pe, kv_latent, k_pe, w_uk, kv_norm_weight, kv_cache, block_table, seq_lens, *,
+           rope_base: float = DEFAULT_ROPE_BASE, rms_eps: float = DEFAULT_RMS_EPS, table=None,
+           q_latent=None, q_rope=None, status=None, stream=None):
+    """The MLA prolog slice (``mla_prolog``): absorbed query, RoPE, cache append.
+
+    Shapes: q_nope [B][s_q][128][128], q_pe [B][s_q][128][64], kv_latent [B][s_q][512],
+    k_pe [B][s_q][64], w_uk [128][128][512], kv_norm_weight [512] (all bf16);
+    kv_cache [pages][64][576] bf16 is updated in place; block_table [B][max_pages]
+    and seq_lens [B] int32.  table: a rope_table() tensor; without one, the table of
+    rope_base is built once per device and kept.  Returns (q_latent, q_rope, status):
+    status is a one-element int32 device tensor of MLA_DEV_* bits (zeroed here, on the
+    stream, unless the caller passes its own).
+    """
+    import torch
+    if q_nope.dim() != 4:
+        raise ValueError("q_nope must be [batch][s_q][heads][128]")
+    B, S = q_nope.shape[0], q_nope.shape[1]
+    dev = q_nope.device
+    _req(q_nope, "q_nope", torch.bfloat16, (B, S, NUM_HEADS, D_NOPE), dev)
+    _req(q_pe, "q_pe", torch.bfloat16, (B, S, NUM_HEADS, D_ROPE), dev)
+    _req(kv_latent, "kv_latent", torch.bfloat16, (B, S, D_LATENT), dev)
+    _req(k_pe, "k_pe", torch.bfloat16, (B, S, D_ROPE), dev)
+    _req(w_uk, "w_uk", torch.bfloat16, (NUM_HEADS, D_NOPE, D_LATENT), dev)
+    _req(kv_norm_weight, "kv_norm_weight", torch.bfloat16, (D_LATENT,), dev)
+    _req(kv_cache, "kv_cache", torch.bfloat16, None, dev)
+    if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE_SIZE, D_LATENT + D_ROPE):
+        raise ValueError("kv_cache must be [num_pages][64][576]")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch][max_pages_per_seq]")
+    _req(block_table, "block_table", torch.int32, None, dev)
+    _req(seq_lens, "seq_lens", torch.int32, (B,), dev)
+    if q_latent is None:
+        q_latent = torch.empty((B, S, NUM_HEADS, D_LATENT), dtype=torch.bfloat16, device=dev)
+    if q_rope is None:
+        q_rope = torch.empty((B, S, NUM_HEADS, D_ROPE), dtype=torch.bfloat16, device=dev)
+    _req(q_latent, "q_latent", torch.bfloat16, (B, S, NUM_HEADS, D_LATENT), dev)
+    _req(q_rope, "q_rope", torch.bfloat16, (B, S, NUM_HEADS, D_ROPE), dev)
+    with torch.cuda.device(dev):
+        if table is None:
+            key = (dev.index, float(rope_base))
+            table = _rope_tables.get(key)
+            if table is None:
+                table = _rope_tables[key] = rope_table(rope_base, dev, stream)
+        _req(table, "table", torch.float32, (ROPE_TABLE_FLOATS,), dev)
+        if status is None:
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+        _req(status, "status", torch.int32, (1,), dev)
+        prob = _problem(B, S, block_table.shape[1])
+        _check(load_library().mla_prolog(
+            ctypes.byref(prob), q_nope.data_ptr(), q_pe.data_ptr(), kv_latent.data_ptr(),
+            k_pe.data_ptr(), w_uk.data_ptr(), kv_norm_weight.data_ptr(), float(rms_eps),
+            table.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], block_table.data_ptr(),
+            seq_lens.data_ptr(), q_latent.data_ptr(), q_rope.data_ptr(), status.data_ptr(),
+            _stream_handle(stream)), "mla_prolog")
+    return q_latent, q_rope, status
 
 
 def check(p: Plan, stream=None) -> int:

@@ -46,7 +46,7 @@ def absorb_q(q_nope, w_uk) -> np.ndarray:
     """q_latent[t, h, :] = q_nope[t, h, :] · W_UK[h]  ([T, H, dn] x [H, dn, dl] -> [T, H, dl])."""
     q = _f64(q_nope)
     w = _f64(w_uk)
-    return np.einsum("thk,hkn->thn", q, w)
+    return np.matmul(q.transpose(1, 0, 2), w).transpose(1, 0, 2)   # per head: [T, dn] @ [dn, dl]
 
 
 def rope_angles(pos, d_rope: int, base: float) -> np.ndarray:

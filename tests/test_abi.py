@@ -12,18 +12,22 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 def _declared():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mla_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = _declared()
     for required in ["mla_decode_plan", "mla_decode", "mla_decode_workspace_size",
-                     "mla_decode_check", "mla_status_string"]:
+                     "mla_decode_check", "mla_status_string", "mla_prolog"]:
         assert required in names
 
 
@@ -46,9 +50,10 @@ def test_status_strings():
     assert lib.mla_status_string(99) == b"unknown status"
 
 
-def test_header_compiles_as_c():
+@pytest.mark.parametrize("header", HEADERS, ids=os.path.basename)
+def test_header_compiles_as_c(header):
     cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c",
-                         HEADER], capture_output=True, text=True)
+                         "-I", os.path.dirname(header), header], capture_output=True, text=True)
     assert cc.returncode == 0, cc.stderr
 
 

@@ -23,6 +23,14 @@ Workloads (the pages' decode shapes; see the design notes for the citations):
     mixed     B=64,  s_q=1, 26 x 20480 + 38 x 400 interleaved at random
     long      B=4,   s_q=1, 4 x 262144
     long1m    B=1,   s_q=1, 1 x 1048576
+
+Prolog inputs (the step before attention, ``prolog_tensors``):
+    q_nope [B][s_q][128][128], q_pe [B][s_q][128][64], kv_latent [B][s_q][512],
+    k_pe [B][s_q][64] bf16 ~ N(0, 1); w_uk [128][128][512] bf16 ~ N(0, 1/128)
+    (random weights, unit-variance outputs); kv_norm_weight [512] bf16 ~ 1 + N(0, 0.1^2).
+``sparse_cache`` builds a pool and block table for the append alone: the
+slots of the step's new tokens get distinct pages, every other table entry a
+random page (so positions up to millions need no million-token pool).
 """
 
 from __future__ import annotations
@@ -36,8 +44,11 @@ NUM_HEADS = 128
 D_LATENT = 512
 D_ROPE = 64
 D_ROW = D_LATENT + D_ROPE
+D_NOPE = 128
 PAGE = 64
 SCALE = 192.0 ** -0.5
+ROPE_BASE = 10000.0      # DeepSeek V3/R1 rotary base
+RMS_EPS = 1e-6           # DeepSeek V3/R1 RMSNorm epsilon
 
 
 @dataclass
@@ -83,13 +94,13 @@ def custom(seq_lens, s_q: int = 1, seed: int = 0, name: str = "custom") -> Workl
     return Workload(name, seed, len(seq_lens), s_q, list(int(x) for x in seq_lens))
 
 
-def _randn_bf16(shape, gen: torch.Generator, chunk: int = 1 << 26) -> torch.Tensor:
-    """N(0,1) fp32 draws rounded to bf16 (round to nearest even), drawn in chunks."""
+def _randn_bf16(shape, gen: torch.Generator, chunk: int = 1 << 26, std: float = 1.0) -> torch.Tensor:
+    """N(0, std^2) fp32 draws rounded to bf16 (round to nearest even), drawn in chunks."""
     n = math.prod(shape)
     out = torch.empty(n, dtype=torch.bfloat16)
     for i in range(0, n, chunk):
         m = min(chunk, n - i)
-        out[i:i + m] = torch.randn(m, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+        out[i:i + m] = (torch.randn(m, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
     return out.view(*shape)
 
 
@@ -147,3 +158,49 @@ def flops(seq_lens, s_q: int) -> int:
     """Tensor FLOPs of one step: 2 * heads * (576 + 512) per (query token, visible key)."""
     per_key = 2 * NUM_HEADS * (D_ROW + D_LATENT)
     return sum(per_key * (int(L) - s_q + 1 + t) for L in seq_lens for t in range(s_q))
+
+
+def prolog_tensors(batch: int, s_q: int, seed: int) -> dict:
+    """Raw per-token inputs and weights of one prolog step (bf16, CPU)."""
+    gen = torch.Generator().manual_seed(seed + 2000)
+    return {
+        "q_nope": _randn_bf16((batch, s_q, NUM_HEADS, D_NOPE), gen),
+        "q_pe": _randn_bf16((batch, s_q, NUM_HEADS, D_ROPE), gen),
+        "kv_latent": _randn_bf16((batch, s_q, D_LATENT), gen),
+        "k_pe": _randn_bf16((batch, s_q, D_ROPE), gen),
+        "w_uk": _randn_bf16((NUM_HEADS, D_NOPE, D_LATENT), gen, std=D_NOPE ** -0.5),
+        "kv_norm_weight": (1.0 + 0.1 * torch.randn(D_LATENT, generator=gen)).to(torch.bfloat16),
+    }
+
+
+def sparse_cache(seq_lens, s_q: int, seed: int, extra_pages: int = 4) -> dict:
+    """Cache pool, block table and seq_lens for an append-only step (see the module notes)."""
+    gen = torch.Generator().manual_seed(seed + 3000)
+    B = len(seq_lens)
+    max_pages = max(1, max((int(L) + PAGE - 1) // PAGE for L in seq_lens))
+    slots = sorted({(b, (int(L) - s_q + t) // PAGE) for b, L in enumerate(seq_lens)
+                    for t in range(s_q) if int(L) - s_q + t >= 0})
+    pool = len(slots) + extra_pages
+    block_table = torch.randint(0, pool, (B, max_pages), generator=gen, dtype=torch.int32)
+    perm = torch.randperm(pool, generator=gen).to(torch.int32)
+    for k, (b, j) in enumerate(slots):
+        block_table[b, j] = perm[k]
+    return {
+        "kv_cache": _randn_bf16((pool, PAGE, D_ROW), gen),
+        "block_table": block_table,
+        "seq_lens": torch.tensor([int(L) for L in seq_lens], dtype=torch.int32),
+    }
+
+
+def prolog_bytes(batch: int, s_q: int) -> int:
+    """Algorithmic HBM bytes of one prolog launch: every input read once, every output written once."""
+    T = batch * s_q
+    reads = 2 * (T * NUM_HEADS * (D_NOPE + D_ROPE) + NUM_HEADS * D_NOPE * D_LATENT
+                 + T * (D_LATENT + D_ROPE) + D_LATENT) + 4 * (batch + T)   # + seq_lens, table entries
+    writes = 2 * (T * NUM_HEADS * (D_LATENT + D_ROPE) + T * D_ROW)
+    return reads + writes
+
+
+def prolog_flops(batch: int, s_q: int) -> int:
+    """Tensor FLOPs of the absorbed-q contraction: 2 x tokens x heads x 128 x 512."""
+    return 2 * batch * s_q * NUM_HEADS * D_NOPE * D_LATENT
