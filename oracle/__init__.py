@@ -20,6 +20,10 @@ library softmax on tiny inputs, closed forms, and invariants.
 ``oracle.prolog`` (numpy, fp64) holds the step before attention: the
 absorbed query projection, RoPE, RMSNorm of the new latent and the append
 into the paged cache; its pins are in ``tests/test_prolog_pins.py``.
+``oracle.epilog`` (numpy, fp64) holds the step after it: the value
+up-projection W_UV per head, the output projection W_O, and the same layer
+written as plain (unabsorbed) multi-head attention; pins in
+``tests/test_epilog_pins.py``.
 """
 
 from __future__ import annotations
