@@ -9,6 +9,7 @@ seq_len 4096); ``--workload`` picks another for manual runs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
     python bench.py --stage prolog [--workload W]     # the step before attention, alone
+    python bench.py --stage epilog [--workload W]     # the step after it (W_UV, o_proj), alone
 
 Prints one JSON line.  ``value`` is KV-cache TB/s (algorithmic bytes: every
 cached row once, 1152 B per key) over all ranks; TFLOPS, microseconds per
@@ -37,6 +38,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode KV-cache TB/s, TFLOPS and % of GB300 roofline; µs per decode step"
+EPILOG_METRIC = "MLA epilog (W_UV per head, o_proj) algorithmic HBM GB/s; µs per step"
 PROLOG_METRIC = "MLA prolog (absorbed q, RoPE, RMSNorm, paged append) algorithmic HBM GB/s; µs per launch"
 NOMINAL_HBM_TBS = 8.0
 L2_FLUSH_BYTES = 256 << 20
@@ -51,8 +53,9 @@ def _args():
                     help="timed steps (default: enough for ~3 s of timed work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--stage", choices=["decode", "prolog"], default="decode",
-                    help="decode: the attention step (default); prolog: the step before it alone")
+    ap.add_argument("--stage", choices=["decode", "prolog", "epilog"], default="decode",
+                    help="decode: the attention step (default); prolog / epilog: the step before / "
+                         "after it alone")
     ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -639,6 +642,118 @@ def run_prolog(args, rank, world, local):
     return 0
 
 
+def run_epilog(args, rank, world, local):
+    """--stage epilog: the W_UV step (hand-written tcgen05 kernel) and o_proj (cuBLASLt).
+
+    The workload's tokens (batch x s_q); L2 flushed (256 MiB written) before every
+    step; events around each of the two launches, all K steps in one CUDA graph.
+    value = algorithmic bytes of both / step time; the roofline is the W_UV kernel's.
+    """
+    import torch
+    import mla_decode_attention_02_gb300 as mla
+
+    if world > 1:
+        raise SystemExit("--stage epilog runs on one GPU")
+    w = W.workload(args.workload)
+    B, S = w.batch, w.s_q
+    T = B * S
+    uv_b, op_b = W.epilog_bytes(T)
+    if args.impl == "reference":
+        from oracle import epilog as OE
+        e = W.epilog_tensors(T, w.seed)
+        times = []
+        for _ in range(max(1, args.steps or 2)):
+            t0 = time.perf_counter()
+            OE.o_project(OE.uv_project(e["o_latent"], e["w_uv"]), e["w_o"])
+            times.append(time.perf_counter() - t0)
+        sec = statistics.median(times)
+        print(json.dumps({"metric": EPILOG_METRIC, "stage": "epilog", "impl": "reference",
+                          "value": (uv_b + op_b) / sec / 1e9, "unit": "GB/s", "us_per_step": sec * 1e6,
+                          "higher_is_better": True, "n_gpus": 1, "dtype": "f64",
+                          "config": {"workload": w.name, "tokens": T}}), flush=True)
+        return 0
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    e = {k: v.to(dev) for k, v in W.epilog_tensors(T, w.seed).items()}
+    o_lat = e["o_latent"].view(B, S, W.NUM_HEADS, W.D_LATENT)
+    o_v = torch.empty((B, S, W.NUM_HEADS, W.D_V), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, W.HIDDEN), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mla.epilog_oproj_workspace_size(), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        mla.epilog_uv(o_lat, e["w_uv"], o_v=o_v, status=status)
+        mla.epilog_oproj(o_v, e["w_o"], out=out, workspace=ws)
+    torch.cuda.synchronize()
+    steps = args.steps or 200
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk(), mk()) for _ in range(steps)]
+    for trio in ev:
+        for x in trio:
+            x.record()
+    torch.cuda.synchronize()
+
+    def timed(external: bool):
+        cur = torch.cuda.current_stream()
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            _record(ev[k][0], cur, external)
+            mla.epilog_uv(o_lat, e["w_uv"], o_v=o_v, status=status)
+            _record(ev[k][1], cur, external)
+            mla.epilog_oproj(o_v, e["w_o"], out=out, workspace=ws)
+            _record(ev[k][2], cur, external)
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            timed(external=True)
+        torch.cuda.synchronize()
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.5)
+    t_start = time.time()
+    if graph is not None:
+        graph.replay()
+    else:
+        timed(external=False)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    clocks = sampler.summary(t_start, t_end)
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} in the epilog")
+    uv_us = statistics.mean(_event_ms(a, b) * 1e3 for a, b, _ in ev)
+    op_us = statistics.mean(_event_ms(b, c) * 1e3 for _, b, c in ev)
+    step_us = uv_us + op_us
+    peaks, peak_src = _peaks()
+    uv_gbs = uv_b / (uv_us * 1e-6) / 1e9
+    op_gbs = op_b / (op_us * 1e-6) / 1e9
+    line = {"metric": EPILOG_METRIC, "stage": "epilog",
+            "value": (uv_b + op_b) / (step_us * 1e-6) / 1e9, "unit": "GB/s", "us_per_step": step_us,
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "s_q": S, "tokens": T, "hidden": W.HIDDEN,
+                       "l2": "flushed (256 MiB written) before every step"},
+            "phases_us": {"uv": uv_us, "oproj": op_us},
+            "oproj": {"library": "cuBLASLt", "achieved_gbs": op_gbs, "frac": op_gbs / peaks["hbm_gbs"],
+                      "algorithmic_bytes": op_b},
+            "roofline": {"kernel": "mla_epilog_uv", "bound": "hbm", "achieved": uv_gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": uv_gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peak_src, "algorithmic_bytes_per_launch": uv_b},
+            "gpu_launches": steps, "clocks": clocks, "launch": "eager" if args.no_graph else "cuda_graph",
+            "device": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = _args()
     rank, world, local = _dist()
@@ -646,6 +761,8 @@ def main():
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.stage == "prolog":
         return run_prolog(args, rank, world, local)
+    if args.stage == "epilog":
+        return run_epilog(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_native(args, rank, world, local)

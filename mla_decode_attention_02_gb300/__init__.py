@@ -13,15 +13,22 @@ q_rope and appends the step's rows to the cache:
 
     q_latent, q_rope, st = prolog(q_nope, q_pe, kv_latent, k_pe, w_uk, gamma,
                                   kv_cache, block_table, seq_lens)   # mla_prolog
+
+and the step after it (``include/mla_epilog.h``) projects the heads back out:
+
+    o_v, st = epilog_uv(o_latent, w_uv)                      # mla_epilog_uv
+    out = epilog_oproj(o_v, w_o)                             # mla_epilog_oproj
 """
 
-from ._binding import (DEFAULT_ROPE_BASE, DEFAULT_RMS_EPS, DEFAULT_SCALE, D_LATENT, D_NOPE, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
+from ._binding import (D_V, HIDDEN, DEFAULT_ROPE_BASE, DEFAULT_RMS_EPS, DEFAULT_SCALE, D_LATENT, D_NOPE, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
                        MLA_DEV_BAD_PAGE, MLA_DEV_BAD_PLAN, MLA_DEV_BAD_SEQ_LEN, MLA_DEV_TIMEOUT,
                        MLAError, NOALLOC_SCRATCH_BYTES, Plan, check, decode, decode_noalloc,
+                       epilog_oproj, epilog_oproj_workspace_size, epilog_uv,
                        load_library, num_units, parse_plan, plan, prolog, rope_table,
                        plan_device_bytes, plan_host, plan_layout, workspace_size)
 
-__all__ = ["DEFAULT_ROPE_BASE", "DEFAULT_RMS_EPS", "DEFAULT_SCALE", "D_LATENT", "D_NOPE", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
+__all__ = ["D_V", "HIDDEN", "epilog_oproj", "epilog_oproj_workspace_size", "epilog_uv",
+           "DEFAULT_ROPE_BASE", "DEFAULT_RMS_EPS", "DEFAULT_SCALE", "D_LATENT", "D_NOPE", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
            "MLA_DEV_BAD_PAGE", "MLA_DEV_BAD_PLAN", "MLA_DEV_BAD_SEQ_LEN", "MLA_DEV_TIMEOUT",
            "MLAError", "NOALLOC_SCRATCH_BYTES", "Plan", "check", "decode", "decode_noalloc",
            "load_library", "num_units", "parse_plan",

@@ -65,6 +65,10 @@ _SIGS = {
     "mla_prolog": (ctypes.c_int, [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                   _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mla_prolog_rope_table": (ctypes.c_int, [ctypes.c_double, _vp, _vp]),
+    "mla_epilog_uv": (ctypes.c_int, [_P, _vp, _vp, _vp, _vp, _vp]),
+    "mla_epilog_oproj_workspace_size": (ctypes.c_size_t, []),
+    "mla_epilog_oproj": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp,
+                                        ctypes.c_size_t, _vp]),
 }
 
 
@@ -324,6 +328,71 @@ def prolog(q_nope, q_pe, kv_latent, k_pe, w_uk, kv_norm_weight, kv_cache, block_
             seq_lens.data_ptr(), q_latent.data_ptr(), q_rope.data_ptr(), status.data_ptr(),
             _stream_handle(stream)), "mla_prolog")
     return q_latent, q_rope, status
+
+
+D_V = 128
+HIDDEN = 7168
+
+
+def epilog_uv(o_latent, w_uv, *, o_v=None, status=None, stream=None):
+    """The value up-projection (``mla_epilog_uv``): o_v[t][h] = W_UV[h] . o_latent[t][h].
+
+    o_latent [B][s_q][128][512] and w_uv [128][128][512] bf16 -> (o_v [B][s_q][128][128] bf16,
+    status: one-element int32 device tensor of MLA_DEV_* bits).
+    """
+    import torch
+    if o_latent.dim() != 4:
+        raise ValueError("o_latent must be [batch][s_q][heads][512]")
+    B, S = o_latent.shape[0], o_latent.shape[1]
+    dev = o_latent.device
+    _req(o_latent, "o_latent", torch.bfloat16, (B, S, NUM_HEADS, D_LATENT), dev)
+    _req(w_uv, "w_uv", torch.bfloat16, (NUM_HEADS, D_V, D_LATENT), dev)
+    if o_v is None:
+        o_v = torch.empty((B, S, NUM_HEADS, D_V), dtype=torch.bfloat16, device=dev)
+    _req(o_v, "o_v", torch.bfloat16, (B, S, NUM_HEADS, D_V), dev)
+    with torch.cuda.device(dev):
+        if status is None:
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+        _req(status, "status", torch.int32, (1,), dev)
+        prob = _problem(B, S, 1)
+        _check(load_library().mla_epilog_uv(ctypes.byref(prob), o_latent.data_ptr(), w_uv.data_ptr(),
+                                            o_v.data_ptr(), status.data_ptr(), _stream_handle(stream)),
+               "mla_epilog_uv")
+    return o_v, status
+
+
+def epilog_oproj(o_v, w_o, *, out=None, workspace=None, stream=None):
+    """The output projection (``mla_epilog_oproj``, cuBLASLt): out = o_v . W_O^T.
+
+    o_v [..][128][128] bf16 viewed as [tokens][16384], w_o [hidden][16384] bf16 ->
+    out [tokens][hidden] bf16.  workspace: optional uint8 device tensor.
+    """
+    import torch
+    dev = o_v.device
+    tokens = o_v.numel() // (NUM_HEADS * D_V)
+    if tokens * NUM_HEADS * D_V != o_v.numel() or tokens < 1:
+        raise ValueError("o_v must hold whole [128][128] token rows")
+    _req(o_v, "o_v", torch.bfloat16, None, dev)
+    if w_o.dim() != 2 or w_o.shape[1] != NUM_HEADS * D_V:
+        raise ValueError("w_o must be [hidden][16384]")
+    _req(w_o, "w_o", torch.bfloat16, None, dev)
+    hidden = w_o.shape[0]
+    if out is None:
+        out = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
+    _req(out, "out", torch.bfloat16, (tokens, hidden), dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8, None, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    with torch.cuda.device(dev):
+        _check(load_library().mla_epilog_oproj(int(tokens), int(hidden), o_v.data_ptr(), w_o.data_ptr(),
+                                               out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream)),
+               "mla_epilog_oproj")
+    return out
+
+
+def epilog_oproj_workspace_size() -> int:
+    return int(load_library().mla_epilog_oproj_workspace_size())
 
 
 def check(p: Plan, stream=None) -> int:

@@ -69,7 +69,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple = ()) -
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+    # cuBLASLt (the output projection's plain GEMM) is found next to the CUDA runtime
+    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+    cmd = [nvcc, ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-L", libdir, "-lcublasLt",
+           "-Xlinker", "-rpath=" + libdir]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

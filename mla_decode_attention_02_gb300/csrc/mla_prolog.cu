@@ -56,6 +56,8 @@
 #include "sm103_ptx.cuh"
 
 namespace mla {
+bool encode_bf16_4d(CUtensorMap *m, const void *base, cuuint64_t d1, cuuint64_t d2, cuuint64_t d3,
+                    cuuint64_t s1, cuuint64_t s2, cuuint64_t s3, cuuint32_t rows, cuuint32_t blocks);
 namespace {
 using namespace ptx;
 
@@ -360,34 +362,6 @@ __global__ void __launch_bounds__(kThreadsP, 4) mla_prolog_kernel(const __grid_c
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 prolog_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// A rank-4 bf16 view with a 128-byte-swizzled box of (64, rows, blocks, 1).
-bool encode4(CUtensorMap *m, const void *base, cuuint64_t d1, cuuint64_t d2, cuuint64_t d3,
-             cuuint64_t s1, cuuint64_t s2, cuuint64_t s3, cuuint32_t rows, cuuint32_t blocks) {
-    auto fn = prolog_encoder();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {64, d1, d2, d3};
-    const cuuint64_t strides[3] = {s1, s2, s3};
-    const cuuint32_t box[4] = {64, rows, blocks, 1};
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 std::mutex g_prolog_mutex;
 bool g_prolog_attr[64];
 
@@ -455,8 +429,8 @@ extern "C" mla_status mla_prolog(const mla_problem *prob, const void *q_nope, co
     const uint32_t smem = std::max<uint32_t>(kSmemMinP, ((2u * p.a_rows * 128 + 1023u) & ~1023u) + kBBytes + 1024);
     const cuuint64_t H = kHeads, T = (cuuint64_t)tokens;
     // q_nope (dims, tokens, dim blocks, heads); W_UK (cols, dims, col blocks, heads)
-    if (!encode4(&p.tm_a, q_nope, T, kDn / 64, H, H * kDn * 2, 128, kDn * 2, (cuuint32_t)p.a_rows, kDn / 64) ||
-        !encode4(&p.tm_b, w_uk, kDn, kDl / 64, H, kDl * 2, 128, (cuuint64_t)kDn * kDl * 2, kDn, kBN / 64))
+    if (!encode_bf16_4d(&p.tm_a, q_nope, T, kDn / 64, H, H * kDn * 2, 128, kDn * 2, (cuuint32_t)p.a_rows, kDn / 64) ||
+        !encode_bf16_4d(&p.tm_b, w_uk, kDn, kDl / 64, H, kDl * 2, 128, (cuuint64_t)kDn * kDl * 2, kDn, kBN / 64))
         return MLA_ERR_CUDA;
     p.q_pe = static_cast<const __nv_bfloat16 *>(q_pe);
     p.kv_latent = static_cast<const __nv_bfloat16 *>(kv_latent);

@@ -45,6 +45,8 @@ D_LATENT = 512
 D_ROPE = 64
 D_ROW = D_LATENT + D_ROPE
 D_NOPE = 128
+D_V = 128
+HIDDEN = 7168
 PAGE = 64
 SCALE = 192.0 ** -0.5
 ROPE_BASE = 10000.0      # DeepSeek V3/R1 rotary base
@@ -204,3 +206,21 @@ def prolog_bytes(batch: int, s_q: int) -> int:
 def prolog_flops(batch: int, s_q: int) -> int:
     """Tensor FLOPs of the absorbed-q contraction: 2 x tokens x heads x 128 x 512."""
     return 2 * batch * s_q * NUM_HEADS * D_NOPE * D_LATENT
+
+
+def epilog_tensors(tokens: int, seed: int, hidden: int = HIDDEN) -> dict:
+    """Inputs and random weights of the step after attention (bf16, CPU): o_latent ~ N(0, 1),
+    W_UV ~ N(0, 1/512), W_O ~ N(0, 1/16384), so every projection keeps unit variance."""
+    gen = torch.Generator().manual_seed(seed + 4000)
+    return {
+        "o_latent": _randn_bf16((tokens, NUM_HEADS, D_LATENT), gen),
+        "w_uv": _randn_bf16((NUM_HEADS, D_V, D_LATENT), gen, std=D_LATENT ** -0.5),
+        "w_o": _randn_bf16((hidden, NUM_HEADS * D_V), gen, std=(NUM_HEADS * D_V) ** -0.5),
+    }
+
+
+def epilog_bytes(tokens: int, hidden: int = HIDDEN) -> tuple:
+    """Algorithmic HBM bytes of (the W_UV step, o_proj): every input read once, output written once."""
+    uv = 2 * (tokens * NUM_HEADS * (D_LATENT + D_V) + NUM_HEADS * D_V * D_LATENT)
+    op = 2 * (tokens * NUM_HEADS * D_V + hidden * NUM_HEADS * D_V + tokens * hidden)
+    return uv, op
