@@ -11,8 +11,11 @@
 // GB300 design.
 //  - W_UV step (mla_epilog_uv_kernel): one CTA per (head, 128-token tile),
 //    M=128 tokens, N=128 value dims, K=512 latent values in eight 64-value
-//    blocks through a three-stage TMA ring (the q tile's block and W_UV[h]'s
-//    block, both K-major, 128-byte swizzle); warp 0 loads, warp 1 issues
+//    blocks (the tile's block of o_latent and W_UV[h]'s block, both K-major,
+//    128-byte swizzle).  With up to 64 tokens all eight blocks fit in shared
+//    memory and are loaded at once (one CTA per SM, every byte in flight);
+//    with more, they pass through a three-stage ring (two CTAs per SM).
+//    Warp 0 loads, warp 1 issues
 //    four tcgen05.mma (K=16) per block into 128 TMEM columns and frees the
 //    stage with tcgen05.commit; all four warps then read TMEM back (a row
 //    per thread), round to bf16, stage the tile conflict-free in shared
@@ -44,7 +47,8 @@ using namespace ptx;
 
 constexpr int kDv = MLA_D_V;              // value dims per head
 constexpr int kKBlocks = kDl / 64;        // 64-value K blocks of the latent
-constexpr int kStagesE = 3;
+constexpr int kMaxStagesE = kDl / 64;    // the whole K extent in flight
+constexpr int kRingStagesE = 3;          // when it does not fit: a three-stage ring, two CTAs per SM
 constexpr int kThreadsE = 128;
 constexpr uint32_t kBBlkE = kDv * 128;    // one K block of W_UV[h]: 128 rows x 128 B
 constexpr uint32_t kOBlkE = 128 * 128;    // one 64-column block of the staged output tile
@@ -52,13 +56,15 @@ constexpr uint32_t kTmemColsE = kDv;
 constexpr uint32_t kSmemMinE = 48 * 1024; // never five CTAs on an SM (four fill its TMEM)
 constexpr uint64_t kWaitLimitNsE = 2000000000ull;
 static_assert(kDv == 128 && kDl % 64 == 0, "M=128 x N=128 tiles over 64-value K blocks");
+// dynamic shared memory budget: 227 KB per block, less room for the static barriers
+constexpr uint32_t kSmemMaxE = 232448 - 2048;
 
 struct EpilogParams {
     CUtensorMap tm_a;   // o_latent viewed as (64 values, tokens, 8 K blocks, heads)
     CUtensorMap tm_b;   // W_UV viewed as (64 values, 128 rows, 8 K blocks, heads)
     __nv_bfloat16 *o_v;
     int32_t *status;
-    int32_t tokens, a_rows;
+    int32_t tokens, a_rows, stages;
 };
 
 __device__ __forceinline__ bool bounded_wait_e(uint32_t bar, uint32_t parity, int32_t *status) {
@@ -79,7 +85,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kThreadsE, 2) mla_epilog_uv_kernel(const __grid_constant__ EpilogParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[2 * kStagesE + 1];   // full[s], empty[s], done
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStagesE + 1];   // full[s], empty[s], done
     __shared__ uint32_t tmem_slot;
     __shared__ int32_t abort_tile;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -89,11 +95,12 @@ __global__ void __launch_bounds__(kThreadsE, 2) mla_epilog_uv_kernel(const __gri
     const uint32_t a_span = (a_bytes + 1023u) & ~1023u;
     const uint32_t stage_bytes = a_span + kBBlkE;
     const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;
-    const uint32_t b_done = smem_u32(&bars[2 * kStagesE]);
+    const int S = P.stages;
+    const uint32_t b_done = smem_u32(&bars[2 * kMaxStagesE]);
     auto full = [&](int s) { return smem_u32(&bars[s]); };
-    auto empty = [&](int s) { return smem_u32(&bars[kStagesE + s]); };
+    auto empty = [&](int s) { return smem_u32(&bars[kMaxStagesE + s]); };
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStagesE; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
@@ -117,8 +124,8 @@ __global__ void __launch_bounds__(kThreadsE, 2) mla_epilog_uv_kernel(const __gri
             prefetch_tmap(&P.tm_a);
             prefetch_tmap(&P.tm_b);
             for (int kb = 0; kb < kKBlocks; ++kb) {
-                const int s = kb % kStagesE;
-                if (kb >= kStagesE && !bounded_wait_e(empty(s), ((kb / kStagesE) - 1) & 1, P.status)) {
+                const int s = kb % S;
+                if (kb >= S && !bounded_wait_e(empty(s), ((kb / S) - 1) & 1, P.status)) {
                     abort_tile = 1;
                     break;
                 }
@@ -134,8 +141,8 @@ __global__ void __launch_bounds__(kThreadsE, 2) mla_epilog_uv_kernel(const __gri
             constexpr uint32_t idesc = idesc_bf16(128, kDv, 0, 0);
             bool ok = true;
             for (int kb = 0; kb < kKBlocks && ok; ++kb) {
-                const int s = kb % kStagesE;
-                if (!bounded_wait_e(full(s), (kb / kStagesE) & 1, P.status)) {
+                const int s = kb % S;
+                if (!bounded_wait_e(full(s), (kb / S) & 1, P.status)) {
                     ok = false;
                     break;
                 }
@@ -266,12 +273,14 @@ extern "C" mla_status mla_epilog_uv(const mla_problem *prob, const void *o_laten
     EpilogParams p{};
     p.a_rows = tokens >= 128 ? 128 : (int32_t)((tokens + 7) / 8 * 8);
     const uint32_t stage = (((uint32_t)p.a_rows * 128 + 1023u) & ~1023u) + kBBlkE;
-    const uint32_t smem = std::max<uint32_t>(kSmemMinE, kStagesE * stage + 1024);
+    // the whole K extent in flight when it fits (one CTA per SM), else a ring
+    p.stages = kMaxStagesE * stage + 1024 <= kSmemMaxE ? kMaxStagesE : kRingStagesE;
+    const uint32_t smem = std::max<uint32_t>(kSmemMinE, p.stages * stage + 1024);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!g_attr[dev]) {
             if (cudaFuncSetAttribute(mla_epilog_uv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(kStagesE * (16384 + kBBlkE) + 1024)) != cudaSuccess)
+                                     (int)kSmemMaxE) != cudaSuccess)
                 return MLA_ERR_CUDA;
             g_attr[dev] = true;
         }
