@@ -66,3 +66,47 @@ def test_missing_library_fails_loudly(tmp_path):
             b.load_library(str(tmp_path / "nope.so"))
     finally:
         b._lib = saved
+
+
+def _prob(batch=2, s_q=1, heads=128, page=64, max_pages=4):
+    import mla_decode_attention_02_gb300._binding as b
+    return b._Problem(batch, s_q, heads, page, max_pages, 0)
+
+
+def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
+    """Host-side validation of the prolog and epilog entry points (no GPU needed: each call
+    fails on its arguments and returns before touching CUDA)."""
+    import ctypes
+    import mla_decode_attention_02_gb300 as m
+    lib = m.load_library()
+    A = 0x10000                      # a 16-byte aligned address that is never dereferenced
+    ok = [A] * 6
+    good = _prob()
+
+    def prolog(prob, ptrs=ok, eps=1e-6, table=A, num_pages=8, status=A):
+        return lib.mla_prolog(ctypes.byref(prob) if prob is not None else None, *ptrs, eps, table, A,
+                              num_pages, A, A, A, A, status, None)
+    assert prolog(None) == 1
+    assert prolog(_prob(s_q=3)) == 2
+    assert prolog(_prob(heads=64)) == 2
+    assert prolog(_prob(page=32)) == 2
+    assert prolog(_prob(batch=0)) == 1
+    assert prolog(good, ptrs=[A, A + 8, A, A, A, A]) == 1          # q_pe not 16-byte aligned
+    assert prolog(good, eps=-1.0) == 1
+    assert prolog(good, eps=float("nan")) == 1
+    assert prolog(good, table=None) == 1
+    assert prolog(good, num_pages=0) == 1
+    assert prolog(good, status=None) == 1
+    assert lib.mla_prolog_rope_table(-1.0, A, None) == 1
+    assert lib.mla_prolog_rope_table(float("inf"), A, None) == 1
+    assert lib.mla_prolog_rope_table(10000.0, None, None) == 1
+
+    assert lib.mla_epilog_uv(None, A, A, A, A, None) == 1
+    assert lib.mla_epilog_uv(ctypes.byref(_prob(s_q=3)), A, A, A, A, None) == 2
+    assert lib.mla_epilog_uv(ctypes.byref(good), A, A, None, A, None) == 1
+    assert lib.mla_epilog_uv(ctypes.byref(good), A, A, A, None, None) == 1
+    assert lib.mla_epilog_oproj(0, 7168, A, A, A, None, 0, None) == 1
+    assert lib.mla_epilog_oproj(4, 7, A, A, A, None, 0, None) == 1
+    assert lib.mla_epilog_oproj(4, 7168, A + 2, A, A, None, 0, None) == 1
+    assert lib.mla_epilog_oproj(4, 7168, A, A, A, None, 1024, None) == 1   # workspace bytes, no pointer
+    assert lib.mla_epilog_oproj_workspace_size() == 32 << 20
