@@ -10,6 +10,7 @@ seq_len 4096); ``--workload`` picks another for manual runs.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
     python bench.py --stage prolog [--workload W]     # the step before attention, alone
     python bench.py --stage epilog [--workload W]     # the step after it (W_UV, o_proj), alone
+    python bench.py --stage layer [--workload W]      # prolog, decode and epilog in one step
 
 Prints one JSON line.  ``value`` is KV-cache TB/s (algorithmic bytes: every
 cached row once, 1152 B per key) over all ranks; TFLOPS, microseconds per
@@ -38,6 +39,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode KV-cache TB/s, TFLOPS and % of GB300 roofline; µs per decode step"
+LAYER_METRIC = "MLA layer step (prolog, decode, epilog) algorithmic HBM GB/s; µs per layer step"
 EPILOG_METRIC = "MLA epilog (W_UV per head, o_proj) algorithmic HBM GB/s; µs per step"
 PROLOG_METRIC = "MLA prolog (absorbed q, RoPE, RMSNorm, paged append) algorithmic HBM GB/s; µs per launch"
 NOMINAL_HBM_TBS = 8.0
@@ -53,7 +55,7 @@ def _args():
                     help="timed steps (default: enough for ~3 s of timed work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--stage", choices=["decode", "prolog", "epilog"], default="decode",
+    ap.add_argument("--stage", choices=["decode", "prolog", "epilog", "layer"], default="decode",
                     help="decode: the attention step (default); prolog / epilog: the step before / "
                          "after it alone")
     ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
@@ -754,6 +756,111 @@ def run_epilog(args, rank, world, local):
     return 0
 
 
+def run_layer(args, rank, world, local):
+    """--stage layer: the whole absorbed MLA layer of one decode step, on one stream.
+
+    prolog (absorbed q, RoPE, cache append) -> plan -> main -> combine -> W_UV -> o_proj,
+    each launch a programmatic dependent of the one before where the library allows it;
+    L2 flushed before every step; K steps in one CUDA graph, events at the step
+    boundaries.  value = algorithmic bytes of all stages / step time.
+    """
+    import torch
+    import mla_decode_attention_02_gb300 as mla
+
+    if world > 1:
+        raise SystemExit("--stage layer runs on one GPU")
+    w = W.workload(args.workload)
+    B, S = w.batch, w.s_q
+    T = B * S
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}
+    t = {k: v.to(dev) for k, v in W.prolog_tensors(B, S, w.seed).items()}
+    e = {k: v.to(dev) for k, v in W.epilog_tensors(1, w.seed).items() if k != "o_latent"}
+    mp = d["block_table"].shape[1]
+    table = mla.rope_table(W.ROPE_BASE, dev)
+    q_lat = torch.empty((B, S, W.NUM_HEADS, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    q_rope = torch.empty((B, S, W.NUM_HEADS, W.D_ROPE), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mla.workspace_size(B, S, mp), dtype=torch.uint8, device=dev)
+    o = torch.empty((B, S, W.NUM_HEADS, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, S, W.NUM_HEADS), dtype=torch.float32, device=dev)
+    o_v = torch.empty((B, S, W.NUM_HEADS, W.D_V), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, W.HIDDEN), dtype=torch.bfloat16, device=dev)
+    ows = torch.empty(mla.epilog_oproj_workspace_size(), dtype=torch.uint8, device=dev)
+    st_p = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_e = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mla.prolog(t["q_nope"], t["q_pe"], t["kv_latent"], t["k_pe"], t["w_uk"], t["kv_norm_weight"],
+                   d["kv_cache"], d["block_table"], d["seq_lens"], table=table, q_latent=q_lat,
+                   q_rope=q_rope, status=st_p)
+        p = mla.plan(d["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
+        mla.decode(p, q_lat, q_rope, d["kv_cache"], d["block_table"], scale=d["scale"], out=o, lse=lse)
+        mla.epilog_uv(o, e["w_uv"], o_v=o_v, status=st_e)
+        mla.epilog_oproj(o_v, e["w_o"], out=out, workspace=ows)
+        return p
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        p = step()
+    torch.cuda.synchronize()
+    steps = args.steps or 100
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for a_, b_ in ev:
+        a_.record()
+        b_.record()
+    torch.cuda.synchronize()
+
+    def timed(external: bool):
+        cur = torch.cuda.current_stream()
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            _record(ev[k][0], cur, external)
+            step()
+            _record(ev[k][1], cur, external)
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            timed(external=True)
+        torch.cuda.synchronize()
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.5)
+    t_start = time.time()
+    if graph is not None:
+        graph.replay()
+    else:
+        timed(external=False)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    clocks = sampler.summary(t_start, t_end)
+    for name, stv in (("prolog", int(st_p.item())), ("decode", mla.check(p)), ("epilog", int(st_e.item()))):
+        if stv != 0:
+            raise RuntimeError(f"device status {stv:#x} in the {name}")
+    us = statistics.mean(_event_ms(a_, b_) * 1e3 for a_, b_ in ev)
+    uv_b, op_b = W.epilog_bytes(T)
+    nbytes = W.prolog_bytes(B, S) + W.cache_bytes(w.seq_lens) + uv_b + op_b
+    print(json.dumps({"metric": LAYER_METRIC, "stage": "layer", "value": nbytes / (us * 1e-6) / 1e9,
+                      "unit": "GB/s", "us_per_step": us, "n_gpus": 1, "steps": steps,
+                      "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+                      "data": "synthetic",
+                      "config": {"workload": w.name, "batch": B, "s_q": S, "tokens": T,
+                                 "l2": "flushed (256 MiB written) before every step"},
+                      "algorithmic_bytes_per_step": nbytes,
+                      "gpu_launches": 6 * steps, "clocks": clocks,
+                      "launch": "eager" if args.no_graph else "cuda_graph",
+                      "device": torch.cuda.get_device_name(dev)}), flush=True)
+    return 0
+
+
 def main():
     args = _args()
     rank, world, local = _dist()
@@ -763,6 +870,8 @@ def main():
         return run_prolog(args, rank, world, local)
     if args.stage == "epilog":
         return run_epilog(args, rank, world, local)
+    if args.stage == "layer":
+        return run_layer(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_native(args, rank, world, local)
