@@ -315,7 +315,13 @@ def prolog(q_nope, q_pe, kv_latent, k_pe, w_uk, kv_norm_weight, kv_cache, block_
             key = (dev.index, float(rope_base))
             table = _rope_tables.get(key)
             if table is None:
-                table = _rope_tables[key] = rope_table(rope_base, dev, stream)
+                # the kept table must hold its values for every later call on any stream
+                if torch.cuda.is_current_stream_capturing():
+                    raise RuntimeError("prolog: build the rotary table with rope_table() before "
+                                       "capturing a CUDA graph, and pass it as table=")
+                table = rope_table(rope_base, dev, stream)
+                (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+                _rope_tables[key] = table
         _req(table, "table", torch.float32, (ROPE_TABLE_FLOATS,), dev)
         if status is None:
             status = torch.zeros(1, dtype=torch.int32, device=dev)
