@@ -400,6 +400,8 @@ extern "C" mla_status mla_prolog(const mla_problem *prob, const void *q_nope, co
     if (prob->s_q != 1 && prob->s_q != 2) return MLA_ERR_UNSUPPORTED;
     if (prob->num_heads != kHeads || prob->page_size != kPage) return MLA_ERR_UNSUPPORTED;
     if ((int64_t)prob->batch * prob->max_pages_per_seq >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
+    // every position (and so every RoPE angle's integer input) stays below 2^31
+    if ((int64_t)prob->max_pages_per_seq * kPage >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
     const int64_t tokens = (int64_t)prob->batch * prob->s_q;
     const int64_t m_tiles = (tokens + kBM - 1) / kBM;
     const int64_t ctas = m_tiles * kHeads * kNParts;

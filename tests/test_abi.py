@@ -91,6 +91,7 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
     assert prolog(_prob(heads=64)) == 2
     assert prolog(_prob(page=32)) == 2
     assert prolog(_prob(batch=0)) == 1
+    assert prolog(_prob(batch=1, max_pages=1 << 25)) == 2                 # positions past 2^31
     assert prolog(good, ptrs=[A, A + 8, A, A, A, A]) == 1          # q_pe not 16-byte aligned
     assert prolog(good, eps=-1.0) == 1
     assert prolog(good, eps=float("nan")) == 1
