@@ -24,6 +24,9 @@ into the paged cache; its pins are in ``tests/test_prolog_pins.py``.
 up-projection W_UV per head, the output projection W_O, and the same layer
 written as plain (unabsorbed) multi-head attention; pins in
 ``tests/test_epilog_pins.py``.
+``oracle.fp8`` holds the e4m3 latent cache format (per-token fp32 scale):
+the quantiser, deciding codes in fp32 as the GPU does, and the
+dequantisation; pins in ``tests/test_fp8_pins.py``.
 """
 
 from __future__ import annotations
