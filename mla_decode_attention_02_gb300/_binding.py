@@ -66,6 +66,7 @@ _SIGS = {
                                   _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mla_prolog_rope_table": (ctypes.c_int, [ctypes.c_double, _vp, _vp]),
     "mla_epilog_uv": (ctypes.c_int, [_P, _vp, _vp, _vp, _vp, _vp]),
+    "mla_cache_quantize_fp8": (ctypes.c_int, [_vp, ctypes.c_int64, _vp, _vp]),
     "mla_epilog_oproj_workspace_size": (ctypes.c_size_t, []),
     "mla_epilog_oproj": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp,
                                         ctypes.c_size_t, _vp]),
@@ -399,6 +400,31 @@ def epilog_oproj(o_v, w_o, *, out=None, workspace=None, stream=None):
 
 def epilog_oproj_workspace_size() -> int:
     return int(load_library().mla_epilog_oproj_workspace_size())
+
+
+FP8_ROW_BYTES = 656
+
+
+def quantize_cache_fp8(kv_cache, *, out=None, stream=None):
+    """The fp8 (e4m3) cache of a bf16 cache (``mla_cache_quantize_fp8``).
+
+    kv_cache [..][576] bf16 -> uint8 [..][656]: per row the 512 e4m3 codes of c_kv / s,
+    k_rope (bf16 bytes), s (fp32), zero padding.
+    """
+    import torch
+    if kv_cache.shape[-1] != D_LATENT + D_ROPE:
+        raise ValueError("kv_cache rows must hold 576 values")
+    _req(kv_cache, "kv_cache", torch.bfloat16, None, None)
+    dev = kv_cache.device
+    shape = tuple(kv_cache.shape[:-1]) + (FP8_ROW_BYTES,)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=dev)
+    _req(out, "out", torch.uint8, shape, dev)
+    rows = kv_cache.numel() // (D_LATENT + D_ROPE)
+    with torch.cuda.device(dev):
+        _check(load_library().mla_cache_quantize_fp8(kv_cache.data_ptr(), int(rows), out.data_ptr(),
+                                                     _stream_handle(stream)), "mla_cache_quantize_fp8")
+    return out
 
 
 def check(p: Plan, stream=None) -> int:
