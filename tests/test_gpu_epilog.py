@@ -103,3 +103,30 @@ def test_absorbed_layer_on_gpu_equals_unabsorbed_attention(s_q):
             errs.append(np.abs(got[b, tq] - ref))
     err = np.stack(errs)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
+
+
+@pytest.mark.parametrize("name", ["uniform", "mtp"])
+def test_epilog_parity_bench_configuration(name):
+    """The inputs bench.py --stage epilog times (same workload and seeds), every element of both steps."""
+    w = W.workload(name)
+    T = w.batch * w.s_q
+    e = W.epilog_tensors(T, w.seed)
+    o_v, st = mla.epilog_uv(e["o_latent"].view(w.batch, w.s_q, 128, 512).cuda(), e["w_uv"].cuda())
+    ws = torch.empty(mla.epilog_oproj_workspace_size(), dtype=torch.uint8, device="cuda")
+    out = mla.epilog_oproj(o_v, e["w_o"].cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_v = E.uv_project(e["o_latent"], e["w_uv"])
+    _within(_np(o_v).reshape(T, 128, 128), ref_v,
+            E.uv_project(np.abs(_np(e["o_latent"])), np.abs(_np(e["w_uv"]))), 512, f"o_v {name}")
+    # o_proj against the oracle's own chain (its fp64 o_v, never the GPU's): the bound adds to
+    # out's rounding and summation terms the GPU o_v's allowed error carried through |W_O|
+    absdot_v = E.uv_project(np.abs(_np(e["o_latent"])), np.abs(_np(e["w_uv"])))
+    bound_v = REL * np.abs(ref_v) + 512 * 2.0 ** -24 * absdot_v + 1e-6
+    w_abs = np.abs(_np(e["w_o"]))
+    ref_o = E.o_project(ref_v, e["w_o"])
+    bound_o = (REL * np.abs(ref_o) + 128 * 128 * 2.0 ** -24 * E.o_project(np.abs(ref_v) + bound_v, w_abs)
+               + E.o_project(bound_v, w_abs) + 1e-6)
+    err = np.abs(_np(out) - ref_o)
+    assert np.isfinite(_np(out)).all() and not (err > bound_o).any(), \
+        f"out {name}: {(err > bound_o).sum()} outside the bound, worst err {err.max():.3e}"

@@ -155,3 +155,12 @@ def test_rope_table(base):
     ref = OP.rope_angles(np.array(1), 64, base) / (2 * np.pi)
     np.testing.assert_allclose(g, ref, rtol=2.0 ** -46, atol=0)
     assert np.all(np.abs(table[32:]) <= np.abs(table[:32]) * 2.0 ** -24)
+
+
+@pytest.mark.parametrize("name", ["uniform", "mtp"])
+def test_prolog_parity_bench_configuration(name):
+    """The inputs bench.py --stage prolog times (same workload, seeds and table), every element."""
+    w = W.workload(name)
+    t = W.prolog_tensors(w.batch, w.s_q, w.seed)
+    c = W.sparse_cache(w.seq_lens, w.s_q, w.seed)
+    _check_all(t, c, w.s_q, base=W.ROPE_BASE, eps=W.RMS_EPS)
