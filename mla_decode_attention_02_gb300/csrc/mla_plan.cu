@@ -10,13 +10,13 @@
 // rows together, whatever the length mix.
 //
 // Every row (request b, query token t) costs pages + kItemCost on a cost
-// line laid out in row order; the line is cut into num_units stretches of
+// line laid out token-major (line_row below); the line is cut into num_units stretches of
 // `target` = ceil(total / num_units).  If no row is much longer than a
 // stretch, rows stay whole and each goes to the unit whose stretch holds its
 // midpoint (no partial outputs, no merge); otherwise each row is cut where a
 // stretch boundary falls inside it (cut_row).  The choice compares the
-// largest unit load without cuts against target + kItemCost + kSplitPenalty.  Rows keep their order, items are
-// emitted in row order, and units come out non-decreasing, so the unit of
+// largest unit load without cuts against target + kItemCost + kSplitPenalty.  Rows keep their line order,
+// items are emitted in that order, and units come out non-decreasing, so the unit of
 // every item follows from prefix sums alone: no atomics, no sorting, and
 // the same bytes on every run.  The host twin below runs the identical
 // integer arithmetic sequentially.
@@ -34,6 +34,16 @@ namespace {
 constexpr int kPlanThreads = 256;   // one CTA; fewer threads make its block-wide barriers cheaper
 static_assert(kPlanThreads % 32 == 0 && kPlanThreads <= 1024, "planner block");
 constexpr size_t kMaxPlanSmem = 200 * 1024;  // per-row working set of the planner kernel
+
+// Row at position k of the cost line: token-major (every request's query token
+// 0, then every request's token 1, ...), so with s_q = 2 the two tokens of a
+// request sit half a line apart and run at the same time on units half the GPU
+// apart, the second reading the request's pages while the first has just
+// brought them into L2 (one pass per token otherwise streams the cache from
+// DRAM twice).  With s_q = 1 this is row order.
+MLA_HD int32_t line_row(int32_t k, int32_t batch, int32_t s_q) {
+    return (k % batch) * s_q + k / batch;
+}
 
 
 // Inclusive block-wide sum of one int64 per thread (kPlanThreads threads, at
@@ -101,7 +111,8 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     }
     __syncthreads();
     for (int32_t base = 0; base < R; base += kPlanThreads) {
-        const int32_t r = base + threadIdx.x;
+        const int32_t k = base + threadIdx.x;
+        const int32_t r = k < R ? line_row(k, batch, s_q) : R;
         int64_t c = 0;
         if (r < R) {
             const int32_t p = row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages);
@@ -123,19 +134,22 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
     __syncthreads();
 
     // Pass 1b: largest unit load if no row is cut (rows on their midpoint units).
-    for (int32_t r = threadIdx.x; r < R; r += kPlanThreads) {
+    for (int32_t k = threadIdx.x; k < R; k += kPlanThreads) {
+        const int32_t r = line_row(k, batch, s_q);
         const int64_t u = mid_unit(s_pos[r], row_cost(s_pages[r]), target, num_units);
-        if (r == 0 || mid_unit(s_pos[r - 1], row_cost(s_pages[r - 1]), target, num_units) != u)
+        const int32_t rp = k > 0 ? line_row(k - 1, batch, s_q) : 0;
+        if (k == 0 || mid_unit(s_pos[rp], row_cost(s_pages[rp]), target, num_units) != u)
             first_pos[u] = s_pos[r];
     }
     __syncthreads();
     {
         int64_t my_max = 0;
-        for (int32_t r = threadIdx.x; r < R; r += kPlanThreads) {
+        for (int32_t k = threadIdx.x; k < R; k += kPlanThreads) {
+            const int32_t r = line_row(k, batch, s_q);
             const int64_t c = row_cost(s_pages[r]);
             const int64_t u = mid_unit(s_pos[r], c, target, num_units);
-            if (r == R - 1 ||
-                mid_unit(s_pos[r + 1], row_cost(s_pages[r + 1]), target, num_units) != u) {
+            const int32_t rn = k < R - 1 ? line_row(k + 1, batch, s_q) : 0;
+            if (k == R - 1 || mid_unit(s_pos[rn], row_cost(s_pages[rn]), target, num_units) != u) {
                 const int64_t load = s_pos[r] + c - first_pos[u];
                 my_max = load > my_max ? load : my_max;
             }
@@ -149,7 +163,8 @@ mla_plan_kernel(const int32_t *__restrict__ seq_lens, uint8_t *__restrict__ ws, 
 
     // Pass 2: pieces per row -> first item and first partial slot; emit the items.
     for (int32_t base = 0; base < R; base += kPlanThreads) {
-        const int32_t r = base + threadIdx.x;
+        const int32_t k = base + threadIdx.x;
+        const int32_t r = k < R ? line_row(k, batch, s_q) : R;
         int64_t n = 0, np = 0;
         if (r < R) {
             n = cut_row(s_pos[r], s_pages[r], target, num_units, split, NoEmit{});
@@ -237,7 +252,8 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
     const int32_t R = L.num_rows;
     int bad = 0;
     int64_t total = 0;
-    for (int32_t r = 0; r < R; ++r) {
+    for (int32_t k = 0; k < R; ++k) {
+        const int32_t r = line_row(k, batch, s_q);
         int32_t p = row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages);
         if (p < 0) bad = 1;
         row_pos[r] = total;
@@ -246,7 +262,8 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
     const int64_t target = total > 0 ? (total + num_units - 1) / num_units : 1;
     // largest unit load if no row is cut (rows on their midpoint units)
     int64_t max_load = 0, run_first = 0, run_unit = -1;
-    for (int32_t r = 0; r < R; ++r) {
+    for (int32_t k = 0; k < R; ++k) {
+        const int32_t r = line_row(k, batch, s_q);
         const int64_t c = row_cost(row_pages(seq_lens[r / s_q], s_q, r % s_q, max_pages));
         const int64_t u = mid_unit(row_pos[r], c, target, num_units);
         if (u != run_unit) {
@@ -258,7 +275,8 @@ mla_status plan_host(const mla_problem *prob, const int32_t *seq_lens, int32_t n
     }
     const bool split = target + kItemCost + kSplitPenalty < max_load;
     int32_t n_items = 0, n_parts = 0, last_unit = -1;
-    for (int32_t r = 0; r < R; ++r) {
+    for (int32_t k = 0; k < R; ++k) {
+        const int32_t r = line_row(k, batch, s_q);
         const int32_t b = r / s_q, t = r % s_q;
         const int32_t p = row_pages(seq_lens[b], s_q, t, max_pages);
         const int32_t n = cut_row(row_pos[r], p, target, num_units, split, NoEmit{});
