@@ -123,3 +123,23 @@ def test_bad_problem_rejected():
     assert e.value.status == 2
     with pytest.raises(m.MLAError):
         m.plan_host([10], s_q=1, max_pages_per_seq=0, num_units=1)
+
+
+def test_cost_line_is_token_major():
+    """Every request's token 0, then every request's token 1: the two tokens of a request lie half
+    a line apart, and for s_q = 1 the line is row order."""
+    w = W.workload("mtp")
+    B = w.batch
+    r = m.plan_host(w.seq_lens, s_q=2, max_pages_per_seq=128, num_units=76)
+    pos = r["row_pos"]
+    line = [(k % B) * 2 + k // B for k in range(2 * B)]
+    assert np.all(np.diff(pos[line]) > 0)
+    # each request's token 1 runs on the unit half the GPU away from its token 0
+    items, unit = r["items"], r["item_unit"]
+    first_unit = {}
+    for (row, _, _, _), u in zip(items.tolist(), unit.tolist()):
+        first_unit.setdefault(row, u)
+    gaps = [first_unit[2 * b + 1] - first_unit[2 * b] for b in range(B)]
+    assert all(36 <= g <= 40 for g in gaps), sorted(set(gaps))
+    r1 = m.plan_host(w.seq_lens[:64], s_q=1, max_pages_per_seq=128, num_units=76)
+    assert np.all(np.diff(r1["row_pos"]) > 0)
