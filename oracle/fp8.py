@@ -102,3 +102,19 @@ def dequantize_cache(fp8_cache) -> np.ndarray:
     rope_bits = c[:, 512:640].copy().view("<u2").astype(np.uint32) << 16
     rope = rope_bits.view(np.float32).astype(np.float64)
     return np.concatenate([lat, rope], axis=1).reshape(lead + (576,))
+
+
+def decode(q_latent, q_rope, fp8_cache, block_table, seq_lens, *, s_q: int, scale: float, rows=None,
+           threads=None):
+    """fp64 decode over an fp8 cache: the attention of ``oracle.decode`` on the dequantised rows.
+
+    This is what a kernel reading the fp8 cache computes up to its own rounding; the gap to the
+    bf16 cache's result is the quantisation error, reported separately.
+    """
+    import torch
+
+    import oracle
+    rows64 = torch.from_numpy(dequantize_cache(fp8_cache))
+    qd = lambda x: x.double() if isinstance(x, torch.Tensor) else torch.from_numpy(np.asarray(x, np.float64))  # noqa: E731
+    return oracle.decode(qd(q_latent), qd(q_rope), rows64, block_table, seq_lens, s_q=s_q, scale=scale,
+                         rows=rows, threads=threads)

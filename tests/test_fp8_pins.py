@@ -70,3 +70,27 @@ def test_quantize_cache_layout_and_scale():
     rng_ = np.abs(ref).max(-1, keepdims=True)
     rel = err / np.where(rng_ > 0, rng_, 1.0)
     assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)             # at most half an e4m3 step: 2^-4 of the row's max
+
+
+def test_decode_over_exact_fp8_cache_equals_bf16_decode():
+    """A cache whose latent values are e4m3 values times a power-of-two scale survives
+    quantisation unchanged, so the fp8 decode must equal the bf16 decode exactly."""
+    import oracle
+    import workloads as W
+    w = W.custom([5, 64, 130], s_q=2, seed=9)
+    inp = W.make_inputs(w)
+    g = np.random.default_rng(9)
+    codes = g.integers(0, 0x7F, size=inp["kv_cache"].shape[:-1] + (512,), dtype=np.int64)   # finite codes
+    vals = F.e4m3_value(codes.astype(np.uint8)) * np.where(g.random(codes.shape) < 0.5, -1, 1)
+    # each row's largest magnitude must be 448 so that its scale is exactly 1 (then every value is kept)
+    vals[..., 0] = 448.0
+    kv = inp["kv_cache"].clone()
+    kv[..., :512] = torch.from_numpy(vals).to(torch.bfloat16)       # e4m3 values are exact in bf16
+    assert np.array_equal(kv[..., :512].double().numpy(), vals)
+    q8 = F.quantize_cache(kv)
+    o8, l8 = F.decode(inp["q_latent"], inp["q_rope"], q8, inp["block_table"], inp["seq_lens"], s_q=2,
+                      scale=inp["scale"])
+    ob, lb = oracle.decode(inp["q_latent"], inp["q_rope"], kv, inp["block_table"], inp["seq_lens"], s_q=2,
+                           scale=inp["scale"])
+    np.testing.assert_array_equal(o8, ob)
+    np.testing.assert_array_equal(l8, lb)
