@@ -756,6 +756,39 @@ def run_epilog(args, rank, world, local):
     return 0
 
 
+def _layer_reference(w):
+    """The layer on the oracle: prolog and epilog whole, decode over a bounded sample of requests
+    (~15 s, as the decode reference arm), its time scaled to the whole batch by cache bytes."""
+    from oracle import epilog as OE
+    from oracle import prolog as OP
+    B, S = w.batch, w.s_q
+    T = B * S
+    inp = W.make_inputs(w)
+    t = W.prolog_tensors(B, S, w.seed)
+    e = W.epilog_tensors(T, w.seed)
+    c = W.sparse_cache(w.seq_lens, S, w.seed)
+    t0 = time.perf_counter()
+    OP.prolog(t["q_nope"], t["q_pe"], t["kv_latent"], t["k_pe"], t["w_uk"], t["kv_norm_weight"],
+              c["kv_cache"], c["block_table"], c["seq_lens"])
+    t_prolog = time.perf_counter() - t0
+    base = _cpu_baseline(w, inp)
+    t_decode = W.cache_bytes(w.seq_lens) / (base["value"] * 1e12)
+    t0 = time.perf_counter()
+    OE.o_project(OE.uv_project(e["o_latent"], e["w_uv"]), e["w_o"])
+    t_epilog = time.perf_counter() - t0
+    uv_b, op_b = W.epilog_bytes(T)
+    nbytes = W.prolog_bytes(B, S) + W.cache_bytes(w.seq_lens) + uv_b + op_b
+    sec = t_prolog + t_decode + t_epilog
+    print(json.dumps({"metric": LAYER_METRIC, "stage": "layer", "impl": "reference",
+                      "value": nbytes / sec / 1e9, "unit": "GB/s", "us_per_step": sec * 1e6,
+                      "higher_is_better": True, "n_gpus": 1, "dtype": "f64",
+                      "config": {"workload": w.name, "tokens": T},
+                      "phases_s": {"prolog": t_prolog, "decode_extrapolated": t_decode,
+                                   "epilog": t_epilog},
+                      "cpu_baseline": dict(base, value=nbytes / sec / 1e9, unit="GB/s")}), flush=True)
+    return 0
+
+
 def run_layer(args, rank, world, local):
     """--stage layer: the whole absorbed MLA layer of one decode step, on one stream.
 
@@ -772,6 +805,8 @@ def run_layer(args, rank, world, local):
     w = W.workload(args.workload)
     B, S = w.batch, w.s_q
     T = B * S
+    if args.impl == "reference":
+        return _layer_reference(w)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}

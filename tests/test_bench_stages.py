@@ -27,3 +27,10 @@ def test_epilog_reference_leg():
     line = _run("--stage", "epilog", "--impl", "reference", "--workload", "tiny", "--steps", "1")
     assert line["impl"] == "reference" and line["stage"] == "epilog"
     assert line["value"] > 0 and line["config"]["tokens"] == 4
+
+
+def test_layer_reference_leg():
+    line = _run("--stage", "layer", "--impl", "reference", "--workload", "tiny")
+    assert line["impl"] == "reference" and line["stage"] == "layer" and line["value"] > 0
+    assert set(line["phases_s"]) == {"prolog", "decode_extrapolated", "epilog"}
+    assert line["cpu_baseline"]["kind"] == "oracle"
