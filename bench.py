@@ -52,7 +52,8 @@ def _args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: enough for ~3 s of timed work)")
+                    help="minimum timed steps (the region is stretched to >= 1.5 s of step time "
+                         "so that the clock sampler sees it)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--stage", choices=["decode", "prolog", "epilog", "layer"], default="decode",
@@ -61,6 +62,8 @@ def _args():
     ap.add_argument("--workload", default="uniform", choices=sorted(W.SEEDS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per_workload lines (mixed, mtp, long, long1m) of the decode stage")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of from one captured CUDA graph")
     return ap.parse_args()
@@ -320,18 +323,28 @@ def _config(w):
                   f"cache {W.cache_bytes(w.seq_lens) / 1e6:.0f} MB"}
 
 
-def run_native(args, rank, world, local):
+PER_WORKLOADS = ("mixed", "mtp", "long", "long1m")
+STEP_KERNELS = 3          # launches per step: planner, main kernel, merge
+
+
+def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool, warmup: int,
+             sampler_gpu=None, cpu=None):
+    """Time plan + decode of workload `w` on `dev`; returns a dict of times and the inputs.
+
+    Two timed regions run the same steps, each step after a 256 MiB L2 flush:
+    (1) events at step boundaries only (the planner, main kernel and merge
+    overlap through programmatic dependent launch, which events between the
+    kernels would serialise); (2) events around each kernel, for the per-kernel
+    times behind the roofline figure.  Steps are captured in a CUDA graph of K
+    steps that is replayed until at least `min_steps` steps and `min_seconds`
+    of step time have run, so that the clock sampler sees the region.
+    """
     import torch
     import torch.distributed as dist
     import mla_decode_attention_02_gb300 as mla
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    w = W.workload(args.workload)
-    cpu = W.make_inputs(w)
+    if cpu is None:
+        cpu = W.make_inputs(w)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
     B, S = w.batch, w.s_q
     mp = d["block_table"].shape[1]
@@ -347,57 +360,48 @@ def run_native(args, rank, world, local):
                    scale=d["scale"], out=out, lse=lse, events=events)
         return p
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         p = step()
     status = mla.check(p)
     if status != 0:
         raise RuntimeError(f"device status {status:#x} during warm-up")
 
-    steps = args.steps
-    if steps is None:
-        for _ in range(2):  # the first pass still pays one-time costs; keep the second
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(5):
-                flush.fill_(1)
-                step()
-            e1.record()
-            torch.cuda.synchronize()
-            per = e0.elapsed_time(e1) / 5 / 1e3
-        steps = int(min(4000 if not args.no_graph else 20000, max(20, 3.0 / max(per, 1e-6))))
-        steps = int(reduce_over_ranks([steps], "min", world, dev)[0])
+    # calibrate: per-step time with the flush, to size the timed region
+    per = 0.0
+    for _ in range(2):  # the first pass still pays one-time costs; keep the second
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            flush.fill_(1)
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / 5 / 1e3
+    want = max(min_steps, int(min_seconds / max(per, 1e-6)) + 1)
+    want = int(reduce_over_ranks([want], "min", world, dev)[0])
+    K = min(want, 1000 if use_graph else want)
+    reps = -(-want // K)
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    ev_s = [mk() for _ in range(steps)]
-    ev_e = [mk() for _ in range(steps)]
-    ev_k = [[mk(), mk(), mk()] for _ in range(steps)]
+    ev_s = [mk() for _ in range(K)]
+    ev_e = [mk() for _ in range(K)]
+    ev_k = [[mk(), mk(), mk()] for _ in range(K)]
     # torch creates each CUDA event on its first record; the timed loop re-records them
     # through the CUDA runtime (and the library, through the C ABI)
     for e in ev_s + ev_e + [x for evs in ev_k for x in evs]:
         e.record(stream)
     torch.cuda.synchronize()
 
-    gpu_id = None
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-
     def timed_steps(external: bool, phases: bool):
         cur = torch.cuda.current_stream()
-        for k in range(steps):
+        for k in range(K):
             flush.fill_(k & 0xFF)
             _record(ev_s[k], cur, external)
             step(events=ev_k[k] if phases else None)
             _record(ev_e[k], cur, external)
 
-    # Two timed regions over the same K steps.  (1) step boundaries only: the
-    # step time (planner, main kernel and merge overlap their launches by
-    # programmatic dependent launch, which events between the kernels would
-    # serialise).  (2) with events around each kernel: the per-kernel times
-    # behind the roofline figure.
     graphs = []
-    if not args.no_graph:
+    if use_graph:
         for phases in (False, True):
             g_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_):
@@ -406,32 +410,95 @@ def run_native(args, rank, world, local):
         torch.cuda.synchronize()
 
     def run_region(phases: bool):
+        """reps x K steps; returns the per-step times (ms) and, with phases, per-kernel times."""
+        steps_ms, main_ms, comb_ms, plan_ms = [], [], [], []
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        if graphs:
-            graphs[1 if phases else 0].replay()
-        else:
-            timed_steps(external=False, phases=phases)
-        torch.cuda.synchronize()
+        for _ in range(reps):
+            if graphs:
+                graphs[1 if phases else 0].replay()
+            else:
+                timed_steps(external=False, phases=phases)
+            torch.cuda.synchronize()
+            steps_ms += [_event_ms(ev_s[k], ev_e[k]) for k in range(K)]
+            if phases:
+                main_ms += [_event_ms(ev_k[k][0], ev_k[k][1]) for k in range(K)]
+                comb_ms += [_event_ms(ev_k[k][1], ev_k[k][2]) for k in range(K)]
+                plan_ms += [_event_ms(ev_s[k], ev_k[k][0]) for k in range(K)]
         if world > 1:
             dist.barrier()
+        return steps_ms, main_ms, comb_ms, plan_ms
 
-    sampler = ClockSampler(gpu_id) if rank == 0 else None
-    time.sleep(0.5)
+    sampler = ClockSampler(sampler_gpu) if sampler_gpu is not False else None
+    if sampler is not None:
+        time.sleep(0.5)
     t_start = time.time()
-    run_region(phases=False)
+    steps_ms, _, _, _ = run_region(phases=False)
     t_end = time.time()
     clocks = sampler.summary(t_start, t_end) if sampler else None
-    step_ms = statistics.mean(_event_ms(ev_s[k], ev_e[k]) for k in range(steps))
-    run_region(phases=True)
-    phase_step_ms = statistics.mean(_event_ms(ev_s[k], ev_e[k]) for k in range(steps))
+    ph_steps, main_l, comb_l, plan_l = run_region(phases=True)
+    step_ms = statistics.mean(steps_ms)
+    vals = [step_ms, statistics.mean(main_l), statistics.mean(comb_l), statistics.mean(plan_l),
+            statistics.mean(ph_steps)]
+    step_ms, main_ms, comb_ms, plan_ms, phase_step_ms = reduce_over_ranks(vals, "max", world, dev)
+    status = mla.check(p)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+    return {"step_ms": step_ms, "main_ms": main_ms, "comb_ms": comb_ms, "plan_ms": plan_ms,
+            "phase_step_ms": phase_step_ms, "steps": K * reps, "clocks": clocks,
+            "d": d, "cpu": cpu, "ws": ws, "out": out, "lse": lse, "flush": flush, "mp": mp,
+            "region_s": t_end - t_start}
 
-    main_ms = statistics.mean(_event_ms(ev_k[k][0], ev_k[k][1]) for k in range(steps))
-    comb_ms = statistics.mean(_event_ms(ev_k[k][1], ev_k[k][2]) for k in range(steps))
-    plan_ms = statistics.mean(_event_ms(ev_s[k], ev_k[k][0]) for k in range(steps))
-    step_ms, main_ms, comb_ms, plan_ms = reduce_over_ranks([step_ms, main_ms, comb_ms, plan_ms], "max",
-                                                           world, dev)
+
+def _roofline(w, main_ms, peaks, peak_src, traffic):
+    cache_b = W.cache_bytes(w.seq_lens)
+    fl = W.flops(w.seq_lens, w.s_q)
+    hbm_peak = peaks["hbm_gbs"]
+    main_gbs = cache_b / (main_ms * 1e-3) / 1e9
+    main_tflops = fl / (main_ms * 1e-3) / 1e12
+    hbm_frac = main_gbs / hbm_peak
+    tensor_frac = main_tflops / peaks["bf16_tflops"]
+    bound = "hbm" if hbm_frac >= tensor_frac else "tensor"
+    return {"kernel": "mla_decode_main", "bound": bound,
+            "achieved": main_gbs if bound == "hbm" else main_tflops,
+            "peak": hbm_peak if bound == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": hbm_frac if bound == "hbm" else tensor_frac,
+            "traffic": traffic, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": cache_b, "flops_per_launch": fl,
+            "launch_ms": main_ms, "hbm_frac": hbm_frac, "tensor_frac": tensor_frac}
+
+
+def run_native(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import mla_decode_attention_02_gb300 as mla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    peaks, peak_src = _peaks()
+
+    w = W.workload(args.workload)
+    min_steps = args.steps if args.steps is not None else 20
+    m = _measure(w, dev, world, min_steps, 1.5, not args.no_graph, args.warmup,
+                 sampler_gpu=gpu_id if rank == 0 else False)
+    step_ms, main_ms = m["step_ms"], m["main_ms"]
+    steps = m["steps"]
+    m_plan_us, m_comb_us, m_phase_us = m["plan_ms"] * 1e3, m["comb_ms"] * 1e3, m["phase_step_ms"] * 1e3
+    m_clocks = m["clocks"]
+    d, cpu, out, lse, ws, flush, mp = m["d"], m["cpu"], m["out"], m["lse"], m["ws"], m["flush"], m["mp"]
+    S = w.s_q
+    stream = torch.cuda.current_stream()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     cache_b = W.cache_bytes(w.seq_lens)
     fl = W.flops(w.seq_lens, S)
@@ -457,6 +524,7 @@ def run_native(args, rank, world, local):
                        scale=d["scale"], out=out, lse=lse)
             o_host.copy_(out, non_blocking=True)
             l_host.copy_(lse, non_blocking=True)
+            return p
 
         for _ in range(3):
             e2e_step()
@@ -466,9 +534,12 @@ def run_native(args, rank, world, local):
         for k in range(k_e2e):
             flush.fill_(k & 0xFF)
             es[k].record(stream)
-            e2e_step()
+            p = e2e_step()
             ee[k].record(stream)
         torch.cuda.synchronize()
+        status = mla.check(p)
+        if status != 0:
+            raise RuntimeError(f"device status {status:#x} in the end-to-end region")
         e2e_ms = statistics.mean(es[k].elapsed_time(ee[k]) for k in range(k_e2e))
         e2e_ms = reduce_over_ranks([e2e_ms], "max", world, dev)[0]
         e2e = {"value": whole_job_tbs(world, cache_b, e2e_ms), "unit": "TB/s",
@@ -478,27 +549,33 @@ def run_native(args, rank, world, local):
                        "pinned host memory and o_latent + lse read back each step; the KV cache "
                        "is device-resident serving state"}
 
-    status = mla.check(p)
-    if status != 0:
-        raise RuntimeError(f"device status {status:#x} after the timed region")
-
-    peaks, peak_src = _peaks()
-    hbm_peak = peaks["hbm_gbs"]
-    main_gbs = cache_b / (main_ms * 1e-3) / 1e9
-    main_tflops = fl / (main_ms * 1e-3) / 1e12
-    hbm_frac = main_gbs / hbm_peak
-    tensor_frac = main_tflops / peaks["bf16_tflops"]
-    bound = "hbm" if hbm_frac >= tensor_frac else "tensor"
-    roof = {"kernel": "mla_decode_main", "bound": bound,
-            "achieved": main_gbs if bound == "hbm" else main_tflops,
-            "peak": hbm_peak if bound == "hbm" else peaks["bf16_tflops"],
-            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-            "frac": hbm_frac if bound == "hbm" else tensor_frac,
-            "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": cache_b, "flops_per_launch": fl,
-            "launch_ms": main_ms, "hbm_frac": hbm_frac, "tensor_frac": tensor_frac}
+    roof = _roofline(w, main_ms, peaks, peak_src, _ncu_traffic(w.name))
     t_roof = max(cache_b / (NOMINAL_HBM_TBS * 1e12), fl / (peaks["bf16_tflops"] * 1e12))
-    t_roof_meas = max(cache_b / (hbm_peak * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+    t_roof_meas = max(cache_b / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+    del m, d, out, lse, ws, flush
+
+    # the other workloads of the pages, measured the same way (shorter regions)
+    per_workload = {}
+    if not args.no_per_workload:
+        for name in PER_WORKLOADS:
+            if name == w.name:
+                continue
+            wk = W.workload(name)
+            r = _measure(wk, dev, world, 20, 0.3, not args.no_graph, 3, sampler_gpu=False)
+            rf = _roofline(wk, r["main_ms"], peaks, peak_src, _ncu_traffic(name))
+            kb = W.cache_bytes(wk.seq_lens)
+            per_workload[name] = {
+                "config": _config(wk), "steps": r["steps"], "us_per_step": r["step_ms"] * 1e3,
+                "tb_s_step": whole_job_tbs(world, kb, r["step_ms"]),
+                "phases_us": {"plan": r["plan_ms"] * 1e3, "main": r["main_ms"] * 1e3,
+                              "combine": r["comb_ms"] * 1e3},
+                "main_roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                     "hbm_frac", "tensor_frac", "traffic")},
+                "step_roofline_frac_measured_peaks":
+                    max(kb / (peaks["hbm_gbs"] * 1e9),
+                        W.flops(wk.seq_lens, wk.s_q) / (peaks["bf16_tflops"] * 1e12)) / (r["step_ms"] * 1e-3)}
+            del r
+            torch.cuda.empty_cache()
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -511,13 +588,12 @@ def run_native(args, rank, world, local):
                 "data": "synthetic", "config": _config(w),
                 "tflops": world * fl / (step_ms * 1e-3) / 1e12,
                 "us_per_step": step_ms * 1e3,
-                "phases_us": {"plan": plan_ms * 1e3, "main": main_ms * 1e3,
-                              "combine": comb_ms * 1e3,
-                              "step_with_phase_events": phase_step_ms * 1e3},
+                "phases_us": {"plan": m_plan_us, "main": main_ms * 1e3, "combine": m_comb_us,
+                              "step_with_phase_events": m_phase_us},
                 "roofline_frac_8tbs": t_roof / (step_ms * 1e-3),
                 "roofline_frac_measured_peaks": t_roof_meas / (step_ms * 1e-3),
-                "e2e": e2e, "gpu_launches": 3 * steps, "roofline": roof,
-                "cpu_baseline": cpu_base, "clocks": clocks,
+                "e2e": e2e, "gpu_launches": STEP_KERNELS * steps, "roofline": roof,
+                "cpu_baseline": cpu_base, "clocks": m_clocks, "per_workload": per_workload,
                 "device": torch.cuda.get_device_name(dev), "units": mla.num_units(),
                 "launch": "eager" if args.no_graph else "cuda_graph"}
         print(json.dumps(line), flush=True)

@@ -130,8 +130,11 @@ mla_status mla_decode_plan(const mla_problem *prob, const int32_t *seq_lens, voi
  * Run the attention for the schedule in `workspace` (built by
  * mla_decode_plan for the same problem): the main kernel, then the LSE
  * merge of split rows.  kv_cache holds num_pages pages; scale multiplies
- * the 576-value dot product (1/sqrt(192) for DeepSeek V3/R1).  Writes
- * o_latent (bf16) and lse (fp32) for every (b, t, h).
+ * the 576-value dot product (1/sqrt(192) for DeepSeek V3/R1) and must be
+ * finite and > 0 (MLA_ERR_INVALID_ARG otherwise).  Writes o_latent (bf16)
+ * and lse (fp32) for every (b, t, h).  Argument errors (null or unaligned
+ * pointers, num_pages < 1, a bad scale, a workspace below the size any
+ * device could need) are found before any CUDA call.
  */
 mla_status mla_decode(const mla_problem *prob, const void *q_latent, const void *q_rope,
                       const void *kv_cache, int64_t num_pages, const int32_t *block_table,

@@ -1,9 +1,10 @@
 """Build the CUDA library libmla_decode.so in-tree with nvcc (sm_103a only).
 
 All translation units compile in parallel and link with -shared; the CUDA
-runtime links statically, the driver API is reached through
-cudaGetDriverEntryPoint, so the library depends on nothing but libc and the
-NVIDIA driver at load time.
+runtime links statically and the driver API is reached through
+cudaGetDriverEntryPoint.  At load time the library needs libc, the NVIDIA
+driver and libcublasLt (the output projection's plain GEMM, found through an
+rpath to the toolkit's lib64).
 """
 
 from __future__ import annotations

@@ -40,7 +40,40 @@ mla_status check_problem(const mla_problem *p) {
     return MLA_OK;
 }
 
+// The smallest workspace any device could need for this problem (one work
+// unit): a workspace below it is refused before any CUDA call.
+size_t workspace_lower_bound(const mla_problem *p) {
+    return mla::plan_layout(p->batch, p->s_q, 1).total;
+}
+
 }  // namespace
+
+namespace mla {
+
+// Every host-side check of a decode call that needs no CUDA call: the
+// problem, the pointers (non-null, 16-byte aligned), the pool size, the
+// scale (finite and > 0: the kernel takes the row maximum of the raw scores
+// as the maximum of the scaled ones) and a lower bound on the workspace.
+// seq_lens is checked when non-null is required (the allocation-free call).
+mla_status check_decode_args(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                             const void *kv_cache, int64_t num_pages, const int32_t *block_table,
+                             const int32_t *seq_lens, bool need_seq_lens, float scale,
+                             const void *o_latent, const float *lse, const void *workspace,
+                             size_t workspace_bytes, bool need_workspace) {
+    mla_status st = check_problem(prob);
+    if (st != MLA_OK) return st;
+    const void *ptrs[] = {q_latent, q_rope, kv_cache, block_table, o_latent, lse};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+    if (need_seq_lens && (!seq_lens || !aligned16(seq_lens))) return MLA_ERR_INVALID_ARG;
+    if (need_workspace && (!workspace || !aligned16(workspace))) return MLA_ERR_INVALID_ARG;
+    if (num_pages < 1 || num_pages > ((int64_t)1 << 31) - 1) return MLA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
+    if (need_workspace && workspace_bytes < workspace_lower_bound(prob)) return MLA_ERR_WORKSPACE;
+    return MLA_OK;
+}
+
+}  // namespace mla
 
 extern "C" {
 
@@ -91,7 +124,9 @@ mla_status mla_decode_plan(const mla_problem *prob, const int32_t *seq_lens, voi
                            size_t workspace_bytes, mla_stream_t stream) {
     mla_status st = check_problem(prob);
     if (st != MLA_OK) return st;
-    if (!seq_lens || !workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+    if (!seq_lens || !aligned16(seq_lens) || !workspace || !aligned16(workspace))
+        return MLA_ERR_INVALID_ARG;
+    if (workspace_bytes < workspace_lower_bound(prob)) return MLA_ERR_WORKSPACE;
     int32_t units = 0;
     if (mla::main_units(&units) != cudaSuccess) return MLA_ERR_CUDA;
     if (!mla::plan_fits(prob->batch * prob->s_q, units)) return MLA_ERR_UNSUPPORTED;
@@ -107,13 +142,10 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
                               const void *kv_cache, int64_t num_pages, const int32_t *block_table,
                               float scale, void *o_latent, float *lse, void *workspace,
                               size_t workspace_bytes, mla_stream_t stream, void *const *events) {
-    mla_status st = check_problem(prob);
+    mla_status st = mla::check_decode_args(prob, q_latent, q_rope, kv_cache, num_pages, block_table,
+                                           nullptr, false, scale, o_latent, lse, workspace,
+                                           workspace_bytes, true);
     if (st != MLA_OK) return st;
-    const void *ptrs[] = {q_latent, q_rope, kv_cache, block_table, o_latent, lse, workspace};
-    for (const void *p : ptrs)
-        if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
-    if (num_pages < 1 || num_pages > ((int64_t)1 << 31) - 1) return MLA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
     int32_t units = 0;
     if (mla::main_units(&units) != cudaSuccess) return MLA_ERR_CUDA;
     if (workspace_bytes < mla::plan_layout(prob->batch, prob->s_q, units).total)

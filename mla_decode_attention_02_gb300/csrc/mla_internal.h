@@ -150,4 +150,12 @@ struct NoEmit {
     MLA_HD void operator()(int32_t, int32_t, int32_t, int32_t) const {}
 };
 
+// Host-side argument checks of a decode call that make no CUDA call
+// (mla_api.cu); shared by mla_decode and the allocation-free entry point.
+mla_status check_decode_args(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                             const void *kv_cache, int64_t num_pages, const int32_t *block_table,
+                             const int32_t *seq_lens, bool need_seq_lens, float scale,
+                             const void *o_latent, const float *lse, const void *workspace,
+                             size_t workspace_bytes, bool need_workspace);
+
 }  // namespace mla

@@ -46,8 +46,14 @@ extern "C" mla_status mla_decode_noalloc(const mla_problem *prob, const void *q_
                                          int64_t num_pages, const int32_t *block_table,
                                          const int32_t *seq_lens, float scale, void *o_latent,
                                          float *lse, mla_stream_t stream) {
+    // Every argument is checked before anything is enqueued: the planner below
+    // would otherwise run (and rewrite the shared array) for a call that
+    // mla_decode then refuses.
+    mla_status st = mla::check_decode_args(prob, q_latent, q_rope, kv_cache, num_pages, block_table,
+                                           seq_lens, true, scale, o_latent, lse, nullptr, 0, false);
+    if (st != MLA_OK) return st;
     size_t need = 0;
-    mla_status st = mla_decode_workspace_size(prob, &need);
+    st = mla_decode_workspace_size(prob, &need);
     if (st != MLA_OK) return st;
     if (need > kScratchBytes) return MLA_ERR_WORKSPACE;
     void *ws = nullptr;

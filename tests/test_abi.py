@@ -114,3 +114,60 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
     assert lib.mla_cache_quantize_fp8(None, 64, A, None) == 1
     assert lib.mla_cache_quantize_fp8(A, 0, A, None) == 1
     assert lib.mla_cache_quantize_fp8(A, 64, A + 4, None) == 1
+
+
+def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
+    """mla_decode_plan, mla_decode, mla_decode_timed and mla_decode_noalloc refuse null or
+    unaligned pointers, an empty page pool, a non-positive or non-finite scale and a workspace
+    below the size any device could need, before they make a CUDA call (so these run without
+    a GPU; a call that passed validation would stop at the first CUDA call instead)."""
+    import mla_decode_attention_02_gb300 as m
+    lib = m.load_library()
+    A = 0x10000
+    good = _prob()
+    big = 1 << 30                       # plenty of workspace bytes
+
+    def plan(prob=good, seq=A, ws=A, nbytes=big):
+        return lib.mla_decode_plan(ctypes.byref(prob) if prob is not None else None, seq, ws, nbytes, None)
+
+    def decode(prob=good, ptrs=(A, A, A), num_pages=8, bt=A, scale=0.072, out=(A, A), ws=A,
+               nbytes=big, timed=False):
+        args = [ctypes.byref(prob) if prob is not None else None, *ptrs, num_pages, bt, scale, *out, ws,
+                nbytes, None]
+        return lib.mla_decode_timed(*args, None) if timed else lib.mla_decode(*args)
+
+    def noalloc(prob=good, ptrs=(A, A, A), num_pages=8, bt=A, seq=A, scale=0.072, out=(A, A)):
+        return lib.mla_decode_noalloc(ctypes.byref(prob) if prob is not None else None, *ptrs,
+                                      num_pages, bt, seq, scale, *out, None)
+
+    assert plan(prob=None) == 1
+    assert plan(prob=_prob(s_q=3)) == 2
+    assert plan(seq=None) == 1
+    assert plan(seq=A + 4) == 1
+    assert plan(ws=None) == 1
+    assert plan(ws=A + 8) == 1
+    assert plan(nbytes=64) == 3
+    for timed in (False, True):
+        assert decode(prob=None, timed=timed) == 1
+        assert decode(prob=_prob(heads=64), timed=timed) == 2
+        assert decode(ptrs=(None, A, A), timed=timed) == 1
+        assert decode(ptrs=(A, A + 2, A), timed=timed) == 1
+        assert decode(ptrs=(A, A, None), timed=timed) == 1
+        assert decode(bt=None, timed=timed) == 1
+        assert decode(out=(A, None), timed=timed) == 1
+        assert decode(out=(A + 8, A), timed=timed) == 1
+        assert decode(ws=None, timed=timed) == 1
+        assert decode(num_pages=0, timed=timed) == 1
+        assert decode(num_pages=-5, timed=timed) == 1
+        assert decode(num_pages=1 << 31, timed=timed) == 1
+        for bad in (0.0, -0.072, float("nan"), float("inf"), float("-inf")):
+            assert decode(scale=bad, timed=timed) == 1, bad
+        assert decode(nbytes=1024, timed=timed) == 3
+    assert noalloc(prob=None) == 1
+    assert noalloc(seq=None) == 1
+    assert noalloc(seq=A + 4) == 1
+    assert noalloc(out=(A, None)) == 1
+    assert noalloc(ptrs=(A, A, None)) == 1
+    assert noalloc(num_pages=0) == 1
+    assert noalloc(scale=-1.0) == 1
+    assert noalloc(scale=float("nan")) == 1
