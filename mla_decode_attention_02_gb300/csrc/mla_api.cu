@@ -22,7 +22,9 @@ bool plan_fits(int32_t rows, int32_t units);
 cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv,
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
-                        int32_t num_units, cudaStream_t stream);
+                        int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags,
+                        cudaStream_t stream);
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // a bounded device wait gives up after 2 s
 }  // namespace mla
 
 namespace {
@@ -141,7 +143,9 @@ mla_status mla_decode_plan(const mla_problem *prob, const int32_t *seq_lens, voi
 static mla_status decode_impl(const mla_problem *prob, const void *q_latent, const void *q_rope,
                               const void *kv_cache, int64_t num_pages, const int32_t *block_table,
                               float scale, void *o_latent, float *lse, void *workspace,
-                              size_t workspace_bytes, mla_stream_t stream, void *const *events) {
+                              size_t workspace_bytes, mla_stream_t stream, void *const *events,
+                              uint64_t wait_limit_ns = mla::kDefaultWaitLimitNs,
+                              uint32_t test_flags = 0) {
     mla_status st = mla::check_decode_args(prob, q_latent, q_rope, kv_cache, num_pages, block_table,
                                            nullptr, false, scale, o_latent, lse, workspace,
                                            workspace_bytes, true);
@@ -165,7 +169,7 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
     if (!mark(0)) return MLA_ERR_CUDA;
     cudaError_t e = mla::launch_main(q_latent, q_rope, kv_cache, num_pages, block_table, scale,
                                      workspace, o_latent, lse, prob->batch, prob->s_q,
-                                     prob->max_pages_per_seq, units, s);
+                                     prob->max_pages_per_seq, units, wait_limit_ns, test_flags, s);
     if (e != cudaSuccess || !mark(1)) return MLA_ERR_CUDA;
     e = mla::launch_combine(workspace, o_latent, lse, prob->batch, prob->s_q, units, s);
     if (e != cudaSuccess || !mark(2)) return MLA_ERR_CUDA;

@@ -39,7 +39,15 @@
 // while it waits for the peer's half of a page, it polls the softmax's
 // barriers of the next pages without blocking.  The copy runs on the same
 // engine as the page loads and arrives about 1 us after issue; the three P
-// slots cover that.
+// slots cover that.  The copy's only completion signal is the receiver's
+// mbarrier, so the receiver counts the halves it got into a word of the
+// sender's shared memory; the sender checks that count before it rescales
+// its own half in place (only when the pair's max rose above the half's own:
+// the first pages of an item).  The count is a relaxed store: the copy has
+// finished reading its source before the receiver can see it complete, the
+// store follows that observation and the in-place writes follow the load
+// that sees the store, so the order holds without a release, which would
+// cost about 0.4 us on every page.
 //
 // TMEM (512 columns): O half [0,256), S [256,288), q [288,512).  Warp roles
 // per CTA: warp 0 loads the K ring and q, warp 2 the V ring; warp 1 issues
@@ -77,7 +85,6 @@ constexpr int kVStages = 2;         // V ring (page parity)
 constexpr int kPSlots = 3;          // P ring (page mod 3)
 constexpr int kPrefetch = 3;        // L2 prefetch distance in pages
 constexpr int kClusterSize = 2;
-constexpr uint16_t kBoth = 0x3;
 constexpr int kHalfTok = 32;                      // tokens of a page per CTA
 constexpr uint32_t kBox = kHalfTok * 128;         // 32 tokens x 64 dims, 128-byte swizzle
 constexpr uint32_t kKStageBytes = 9 * kBox;       // own tokens, dim blocks 0-8 (one TMA box)
@@ -114,12 +121,11 @@ constexpr uint32_t kTmemCols = 512;
 static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: raise the max only when it grows by > 2^8
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,                        // producer (+tx), softmax warps (q in TMEM)
-    B_Q_EMPTY = 1,                       // score issuers of both CTAs done with q
+    B_Q_FULL = 0,                        // softmax warps: q dims 0-447 in TMEM
+    B_Q_EMPTY = 1,                       // this CTA's score MMAs done with the item's q
     B_KFULL = 2,                         // + page parity: K stage landed (+tx)
     B_KEMPTY = B_KFULL + 2,              // + page parity: score MMAs done with the K stage
     B_VFULL = B_KEMPTY + 2,              // + page parity: V stage landed (+tx)
@@ -131,18 +137,19 @@ enum : uint32_t {
     B_SDONE = B_SEMPTY + 1,              // + slot: own P half written
     B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx)
     B_PREADY = B_PMSG + kPSlots,         // + slot: P tile final, PV may run
-    B_PREAD = B_PREADY + kPSlots,        // + slot: the copy to the peer has read this CTA's half
-    B_RESDONE = B_PREAD + kPSlots,       // + page mod kRefLag: agreed max published
+    B_RESDONE = B_PREADY + kPSlots,      // + page mod kRefLag: agreed max published
     B_PVDONE = B_RESDONE + kRefLag,      // + page parity: PV done
     B_PVLAST = B_PVDONE + 2,             // an item's last PV done (one phase per item)
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
     B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
-    B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx, both CTAs' loads)
+    B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx)
     B_QCOPIED = B_QSTAGE + 1,            // item start: softmax warps moved the staged q to TMEM
-    B_COUNT = B_QCOPIED + 1,
+    B_QTILE = B_QCOPIED + 1,             // q dims 448-575 landed in the shared-memory q tile (+tx)
+    B_COUNT = B_QTILE + 1,
 };
-static_assert(B_COUNT * 8 <= 512, "barrier area");
+static_assert(B_COUNT * 8 <= 504, "barrier area");
+constexpr uint32_t kOffPeerGot = 504;   // in the barrier area: this CTA's halves the peer has received
 
 struct Params {
     CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
@@ -158,14 +165,17 @@ struct Params {
     __nv_bfloat16 *o_latent;
     float *lse;
     int64_t num_pages;
+    uint64_t wait_limit_ns;
     float scale_log2;
     int32_t batch, s_q, max_pages, num_units;
+    uint32_t test_flags;
 };
 
 struct Ctl {
     uint32_t bar0;       // shared address of barrier 0
     volatile int *abort; // shared abort flag
     int *status;         // device status word
+    uint64_t limit_ns;   // a wait gives up after this long
 };
 
 __device__ __forceinline__ uint32_t bar(const Ctl &c, uint32_t i) { return c.bar0 + 8u * i; }
@@ -201,7 +211,37 @@ __device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
             const uint64_t t = globaltimer_ns();
             if (t0 == 0) {
                 t0 = t;
-            } else if (t - t0 > kWaitLimitNs) {
+            } else if (t - t0 > c.limit_ns) {
+                fail(c);
+                return false;
+            }
+        }
+    }
+}
+
+// Teardown wait that ignores the abort flag (for copies already in flight,
+// which always land, and acknowledgements of them): bounded by the limit.
+__device__ __forceinline__ void wait_landed(const Ctl &c, uint32_t b, uint32_t parity, int scope = kCta) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!try_wait(b, parity, scope)) {
+        if (globaltimer_ns() - t0 > c.limit_ns) {
+            fail(c);
+            return;
+        }
+    }
+}
+
+// Bounded wait until a word that the peer writes (release store) reaches `target`.
+__device__ __forceinline__ bool wait_count(const Ctl &c, uint32_t addr, uint32_t target) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (__all_sync(0xffffffffu, ld_relaxed_local(addr) >= target)) return true;
+        if ((i & 63) == 63) {
+            if (__any_sync(0xffffffffu, *c.abort != 0)) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > c.limit_ns) {
                 fail(c);
                 return false;
             }
@@ -233,7 +273,6 @@ __device__ bool send_and_wait(const Ctl &c, uint32_t s_p, uint32_t rank, uint32_
                 const uint32_t pmsg_peer = mapa(pmsg, peer);
                 mbar_arrive_expect_tx(pmsg, kMsgBytes);
                 bulk_copy_s2c(mapa(s_pst + rank * kPPart, peer), s_pst + rank * kPPart, kPPart, pmsg_peer);
-                bulk_commit();
             }
             __syncwarp();
             ++sent;
@@ -246,13 +285,28 @@ __device__ bool send_and_wait(const Ctl &c, uint32_t s_p, uint32_t rank, uint32_
             const uint64_t t = globaltimer_ns();
             if (t0 == 0) {
                 t0 = t;
-            } else if (t - t0 > kWaitLimitNs) {
+            } else if (t - t0 > c.limit_ns) {
                 if (elect_one()) fail(c);
                 __syncwarp();
                 return false;
             }
         }
     }
+}
+
+// Zero the latent rows of tokens [valid, 64) of a landed V stage (the four
+// 64-dim blocks of this CTA's output dims, 128-byte rows), one warp, then
+// make the stores visible to the tensor cores.  Out of line: the PV issue
+// loop stays small.
+__device__ __noinline__ void zero_v_tail(uint8_t *vst, int valid, int lane) {
+    const int per_blk = (kPage - valid) * 8;   // 16-byte chunks per dim block
+    for (int idx = lane; idx < 4 * per_blk; idx += 32) {
+        const int blk = idx / per_blk, rem = idx % per_blk;
+        *reinterpret_cast<uint4 *>(vst + blk * kVBlk + (valid + rem / 8) * 128 + (rem % 8) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -291,11 +345,10 @@ __device__ __forceinline__ void scale_p_row(uint8_t *tile, int h, float f) {
 }
 
 // At an item's start q dims 0-255 (four 64-dim blocks, 128 heads each, 128-byte
-// swizzle) come in by TMA, each CTA loading half the blocks into both, through
-// buffers that are free then: blocks 0-1 in the K stage that the item's second
-// page will use (its first page loads into the other one meanwhile), 2-3 in
-// the shared-memory q tile (free once both CTAs' score MMAs of the previous
-// item are done).  Loading q through registers costs one L1 wavefront per head
+// swizzle) come in by TMA through buffers that are free then: blocks 0-1 in the
+// K stage that the item's second page will use (its first page loads into the
+// other one meanwhile), 2-3 in the shared-memory q tile (free once this CTA's
+// score MMAs of the previous item are done).  Loading q through registers costs one L1 wavefront per head
 // row per instruction, so only dims 256-447 take that path, overlapped.
 constexpr int kQStaged = 4;
 __device__ __forceinline__ uint32_t q_stage_off(int b, uint32_t kstage) {
@@ -346,13 +399,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
     ctl.bar0 = s_base + kOffBar;
     ctl.abort = &abort_flag;
     ctl.status = &hdr->status;
+    ctl.limit_ns = P.wait_limit_ns;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(ctl, B_Q_FULL), 1 + 4);
+        *reinterpret_cast<volatile uint32_t *>(smem + kOffBar + kOffPeerGot) = 0;
+        mbar_init(bar(ctl, B_Q_FULL), 4);
+        mbar_init(bar(ctl, B_QTILE), 1);
         mbar_init(bar(ctl, B_QSTAGE), 1);
         mbar_init(bar(ctl, B_QCOPIED), 4);
-        mbar_init(bar(ctl, B_Q_EMPTY), kClusterSize);
+        mbar_init(bar(ctl, B_Q_EMPTY), 1);
         for (int p = 0; p < 2; ++p) {
             mbar_init(bar(ctl, B_KFULL + p), 1);
             mbar_init(bar(ctl, B_KEMPTY + p), 1);
@@ -366,7 +422,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             mbar_init(bar(ctl, B_SDONE + s), 4);
             mbar_init(bar(ctl, B_PMSG + s), 1);
             mbar_init(bar(ctl, B_PREADY + s), 4);
-            mbar_init(bar(ctl, B_PREAD + s), 1);
         }
         mbar_init(bar(ctl, B_SFULL), 1);
         mbar_init(bar(ctl, B_SEMPTY), 4);
@@ -420,7 +475,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         // (both token halves of this CTA's output dims).  Out-of-pool page
         // indices read zeros (TMA bounds fill); the merge warps flag the row.
         const bool kring = warp == 0;
-        uint32_t g = 0;
+        const bool withhold = kring && (P.test_flags & 1u) && unit == 0 && rank == 0;   // test hook
+        uint32_t g = 0, issued = 0;
+        int q_stage_par = -1, q_tile_par = -1;   // parity of the last q copies issued
         bool ok = true;
         for (int i = i_begin; i < i_end && ok; ++i) {
             const WorkItem it = items[i];
@@ -439,48 +496,49 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const uint32_t p = g & 1;
                     if (kring) {
                         if (k0 + kk == 0) {
-                            // Item start: both CTAs' score MMAs of the previous item are
+                            // Item start: this CTA's score MMAs of the previous item are
                             // done, so the K stage of this item's second page and the
                             // shared-memory q tile are free.  Stage q dims 0-255 there
-                            // (see q_stage_off; each CTA loads half the blocks into both)
-                            // beside this page's K load; this item's q dims 448-575
-                            // follow (unicast: the peer may still be copying out of its
-                            // own tile) once the softmax warps moved the staged blocks
-                            // into TMEM.
-                            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1, kCluster)) {
+                            // (see q_stage_off) beside this page's K load; this item's
+                            // q dims 448-575 follow once the softmax warps moved the
+                            // staged blocks into TMEM.
+                            if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) {
                                 ok = false;
                                 break;
                             }
                             if (lane == 0) {
                                 const uint32_t fq = bar(ctl, B_QSTAGE);
                                 mbar_arrive_expect_tx(fq, kQStaged * kQBlk);
-                                for (int b = (int)rank; b < kQStaged; b += 2)
-                                    tma_load_2d_mc(s_base + q_stage_off(b, p ^ 1), &P.tm_q_lat, 64 * b,
-                                                   it.row * kHeads, fq, kBoth);
+                                for (int b = 0; b < kQStaged; ++b)
+                                    tma_load_2d(s_base + q_stage_off(b, p ^ 1), &P.tm_q_lat, 64 * b,
+                                                it.row * kHeads, fq);
                             }
+                            q_stage_par = (int)(ii & 1);
                         }
                         if (g >= 2 && !wait_warp(ctl, bar(ctl, B_KEMPTY + p), ((g >> 1) - 1) & 1)) {
                             ok = false;
                             break;
                         }
-                        if (lane == 0) {
+                        if (lane == 0 && !(withhold && g == 1)) {
                             // one 36 KB box: an SM ingests a few large TMA copies much
                             // faster than many 4 KB ones
                             const uint32_t fa = bar(ctl, B_KFULL + p);
                             mbar_arrive_expect_tx(fa, kKStageBytes);
                             tma_load_4d(s_k + p * kKStageBytes, &P.tm_k, 0, tok_own, 0, page, fa);
                         }
+                        issued = g + 1;
                         if (k0 + kk == 0) {
                             if (!wait_warp(ctl, bar(ctl, B_QCOPIED), ii & 1)) {
                                 ok = false;
                                 break;
                             }
                             if (lane == 0) {
-                                const uint32_t fb = bar(ctl, B_Q_FULL);
+                                const uint32_t fb = bar(ctl, B_QTILE);
                                 mbar_arrive_expect_tx(fb, kQSBytes);
                                 const int y = it.row * kHeads;
                                 tma_load_2d(s_qs, &P.tm_q_lat, kQTDims, y, fb);
                                 tma_load_2d(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb);
+                                q_tile_par = (int)(ii & 1);
                                 // warm L2 for the next item's q
                                 if (i + 1 < i_end) {
                                     for (int b = 0; b < kDl / 64; ++b)
@@ -503,10 +561,23 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             mbar_arrive_expect_tx(fv, kVStageBytes);
                             tma_load_4d(s_v + p * kVStageBytes, &P.tm_v, 0, 0, 4 * (int)rank, page, fv);
                         }
+                        issued = g + 1;
                     }
                     __syncwarp();
                 }
             }
+        }
+        // on a time-out, the copies in flight land before the CTA may exit (each stage's
+        // last load; a load always completes)
+        if (__any_sync(0xffffffffu, *ctl.abort != 0)) {
+            if (lane == 0) {
+                const uint32_t full = kring ? B_KFULL : B_VFULL;
+                for (uint32_t q = issued > 2 ? issued - 2 : 0; q < issued; ++q)
+                    if (!(withhold && q == 1)) wait_landed(ctl, bar(ctl, full + (q & 1)), (q >> 1) & 1);
+                if (q_stage_par >= 0) wait_landed(ctl, bar(ctl, B_QSTAGE), (uint32_t)q_stage_par);
+                if (q_tile_par >= 0) wait_landed(ctl, bar(ctl, B_QTILE), (uint32_t)q_tile_par);
+            }
+            __syncwarp();
         }
     } else if (warp == kQkWarp || warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuers
@@ -526,7 +597,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const WorkItem it = items[i];
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
             const uint32_t ii = (uint32_t)(i - i_begin);
-            if (qk && !wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1)) break;
+            if (qk && (!wait_warp(ctl, bar(ctl, B_Q_FULL), ii & 1) || !wait_warp(ctl, bar(ctl, B_QTILE), ii & 1)))
+                break;
             for (int k = 0; k < n && ok; ++k, ++g) {
                 const uint32_t p = g & 1;
                 if (qk) {
@@ -568,6 +640,12 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         ok = false;
                         break;
                     }
+                    // the masked tail's latent rows in the V stage become zeros, so that
+                    // 0 * garbage stays 0 in PV (the stage has landed: waited above)
+                    if (k == n - 1) {
+                        const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
+                        if (valid_last < kPage) zero_v_tail(smem + kOffV + p * kVStageBytes, valid_last, lane);
+                    }
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
@@ -577,7 +655,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                                    (k == 0 && ks == 0) ? 0u : 1u);
                         mma_commit(bar(ctl, B_PVDONE + p));
                         mma_commit(bar(ctl, B_PEMPTY + ps));
-                        mma_commit_mc(bar(ctl, B_PEMPTY_PEER + ps), peer_mask);
+                        mma_commit_to(bar(ctl, B_PEMPTY_PEER + ps), peer_mask);
                         // the last page's V stage is released by the epilogue, which
                         // stages the output through it
                         if (k != n - 1)
@@ -588,9 +666,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     __syncwarp();
                 }
             }
-            // the score issuer is done with the item's q (in both CTAs' copies)
+            // the score issuer is done with the item's q
             if (ok && qk) {
-                if (elect_one()) mma_commit_mc(bar(ctl, B_Q_EMPTY), kBoth);
+                if (elect_one()) mma_commit(bar(ctl, B_Q_EMPTY));
                 __syncwarp();
             }
         }
@@ -598,9 +676,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         if (elect_one()) {
             const uint32_t drain = bar(ctl, B_DRAIN + (qk ? 0 : 1));
             mma_commit(drain);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
+            wait_landed(ctl, drain, 0);
         }
         __syncwarp();
     } else if (warp >= kSoftmaxWarp0 && warp < kMergeWarp0) {
@@ -628,7 +704,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 uint4 x[24];
 #pragma unroll
                 for (int v = 0; v < 24; ++v) x[v] = src[v];
-                if (!wait_warp(ctl, bar(ctl, B_QSTAGE), ii & 1, kCluster)) break;
+                if (!wait_warp(ctl, bar(ctl, B_QSTAGE), ii & 1)) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int b = 0; b < kQStaged; ++b) q_stage_to_tmem(smem, b, (g & 1) ^ 1u, h, tQ);
@@ -775,23 +851,25 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     // halves of the pages the softmax has finished (up to kPSlots - 1
                     // pages ahead), each as soon as it is ready.
                     if (!send_and_wait(ctl, s_p, rank, peer, sent, total_pages, gp)) { ok = false; break; }
-                    // this CTA's half may be rescaled in place once the copy has read it
-                    if (elect_one()) {
-                        const uint32_t newer = sent - 1 - gp;   // copies issued after this page's
-                        if (newer == 0) bulk_wait_read<0>();
-                        else if (newer == 1) bulk_wait_read<1>();
-                        else bulk_wait_read<2>();
-                        mbar_arrive(bar(ctl, B_PREAD + ps));
-                    }
+                    // the peer's half of this page has landed: its copy out of the peer's
+                    // shared memory is complete (the peer may rescale that half in place)
+                    if (elect_one()) st_relaxed_remote(mapa(s_base + kOffBar + kOffPeerGot, peer), gp + 1);
                     __syncwarp();
                 } else if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) {
                     ok = false;
                     break;
                 }
-                if (!wait_warp(ctl, bar(ctl, B_PREAD + ps), pu & 1)) { ok = false; break; }
                 const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPHalf + h * 8);
                 const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPPart + kPHalf + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
+                // this CTA's own half (the source of its copy to the peer) may be rescaled
+                // in place only once the peer has received it
+                const float own_m = rank == 0 ? h0.x : h1.x;
+                if (__any_sync(0xffffffffu, own_m != NEG_INF && own_m < nref) &&
+                    !wait_count(ctl, s_base + kOffBar + kOffPeerGot, gp + 1)) {
+                    ok = false;
+                    break;
+                }
                 if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, fast_exp2(h0.x - nref));
                 if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPPart, h, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
@@ -821,18 +899,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : fast_exp2(h0.x - nref));
                     const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : fast_exp2(h1.x - nref));
                     l_run = h0.y * f0 + h1.y * f1;
-                    if (valid_last < kPage) {
-                        // zero this CTA's latent rows of the masked tail once they
-                        // landed, so that 0 * garbage stays 0 in PV
-                        if (!wait_warp(ctl, bar(ctl, B_VFULL + par), (gp >> 1) & 1)) { ok = false; break; }
-                        uint8_t *vst = smem + kOffV + par * kVStageBytes;
-                        const int per_blk = (kPage - valid_last) * 8;   // 16-byte chunks per dim block
-                        for (int idx = h; idx < 4 * per_blk; idx += 128) {
-                            const int blk = idx / per_blk, rem = idx % per_blk;
-                            *reinterpret_cast<uint4 *>(vst + blk * kVBlk + (valid_last + rem / 8) * 128 +
-                                                       (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-                        }
-                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -931,14 +997,21 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 if (lane == 0) mbar_arrive(bar(ctl, B_VEMPTY + p_last));
             }
         }
+        // after a time-out, the halves already sent have been received (their copies
+        // out of this CTA's shared memory are complete) before the CTA may exit
+        if (warp == kMergeWarp0 && __any_sync(0xffffffffu, *ctl.abort != 0)) {
+            if (lane == 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_relaxed_local(s_base + kOffBar + kOffPeerGot) < sent &&
+                       globaltimer_ns() - t0 < ctl.limit_ns) {
+                }
+            }
+            __syncwarp();
+        }
     }
 
-    // the bulk copies of warp 8 are complete before this CTA's shared memory goes away
-    if (warp == kMergeWarp0) {
-        if (elect_one()) bulk_wait_all();
-        __syncwarp();
-    }
-    // teardown: both CTAs finish (no multicast or remote arrive in flight) before TMEM is freed
+    // teardown: both CTAs finish (every bulk copy acknowledged, no remote arrive in
+    // flight) before shared memory and TMEM are released
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -1031,7 +1104,8 @@ cudaError_t main_units(int32_t *units) {
 cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv,
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
-                        int32_t num_units, cudaStream_t stream) {
+                        int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags,
+                        cudaStream_t stream) {
     Params p;
     const cuuint64_t qrows = (cuuint64_t)batch * s_q * kHeads;
     {
@@ -1065,6 +1139,8 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     p.o_latent = static_cast<__nv_bfloat16 *>(o_latent);
     p.lse = lse;
     p.num_pages = num_pages;
+    p.wait_limit_ns = wait_limit_ns;
+    p.test_flags = test_flags;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.batch = batch;
     p.s_q = s_q;

@@ -74,6 +74,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// 32-bit relaxed store into another CTA's shared memory and the matching
+// relaxed load of a local word that a peer CTA writes (cluster scope).  A
+// release store at cluster scope waits for every earlier memory operation of
+// the thread; on the per-page path of the main kernel that cost about 0.4 us.
+__device__ __forceinline__ void st_relaxed_remote(uint32_t addr_cluster, uint32_t v) {
+    asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_local(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -163,17 +177,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in cta_mask;
-// each destination CTA's mbarrier (same offset) receives the complete_tx.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, int32_t c0,
-                                               int32_t c1, uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // Bring a tensor tile into L2 ahead of its load (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int32_t c0, int32_t c1, int32_t c2,
                                                 int32_t c3) {
@@ -209,6 +212,9 @@ __device__ __forceinline__ bool elect_one() {
 // Bulk copy from this CTA's shared memory to another CTA's (addresses from
 // mapa for the destination and its mbarrier); 16-byte aligned, size a multiple
 // of 16.  Completes `bytes` of the destination mbarrier's transaction count.
+// Its only completion signal is that mbarrier: the bulk async-group waits
+// (cp.async.bulk.wait_group) do not track this form, so the sender learns that
+// its source has been read only from the receiver.
 __device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
                                               uint32_t mbar_cluster) {
     asm volatile(
@@ -216,21 +222,6 @@ __device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src
             dst_cluster),
         "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
         : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until all but the N most recent bulk-copy groups of this thread have read their sources.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until every bulk copy this thread committed has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 / TMEM
@@ -285,8 +276,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// Same, arriving on the mbarrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+// Same, arriving on the mbarrier at this offset in every CTA of cta_mask: an
+// mbarrier signal to the peer CTA when the MMAs are done (no data moves).
+__device__ __forceinline__ void mma_commit_to(uint32_t bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(bar),
