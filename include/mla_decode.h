@@ -156,6 +156,30 @@ mla_status mla_decode_timed(const mla_problem *prob, const void *q_latent, const
                             size_t workspace_bytes, mla_stream_t stream, void *const *events);
 
 /*
+ * mla_decode with a caller-chosen limit for the bounded waits inside the
+ * main kernel, and an optional injected stall, for testing the time-out path
+ * without a GPU fault.  The pages have no counterpart of this entry point.
+ *  - wait_limit_ns: how long any one wait of the main kernel may last before
+ *    the kernel records MLA_DEV_TIMEOUT and winds down (mla_decode uses 2 s).
+ *    Must lie in [1000, 60e9]; MLA_ERR_INVALID_ARG otherwise.
+ *  - inject: 0, or MLA_INJECT_WITHHOLD_K_LOAD: the first CTA of the work
+ *    unit that runs the schedule's first item never issues the K-stage load
+ *    of its second page, so the waits for it run out (the unit must own two
+ *    pages or more, else nothing is withheld).  The kernel then records MLA_DEV_TIMEOUT, lets every copy
+ *    already in flight land, frees its tensor memory and returns; the rows of
+ *    that unit are left unspecified, the stream and context stay usable, and
+ *    the next call (which rewrites the status word in mla_decode_plan) runs
+ *    normally.  Other bits: MLA_ERR_INVALID_ARG.
+ * With inject == 0 the results are those of mla_decode, bit for bit.
+ */
+#define MLA_INJECT_WITHHOLD_K_LOAD 0x1u
+mla_status mla_decode_diag(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                           const void *kv_cache, int64_t num_pages, const int32_t *block_table,
+                           float scale, void *o_latent, float *lse, void *workspace,
+                           size_t workspace_bytes, mla_stream_t stream, uint64_t wait_limit_ns,
+                           uint32_t inject);
+
+/*
  * Synchronise `stream`, read the device status word from the workspace into
  * *device_status (MLA_DEV_* bits) and return MLA_OK if it is zero,
  * MLA_ERR_TIMEOUT if MLA_DEV_TIMEOUT is set, else MLA_ERR_DEVICE_CHECK.

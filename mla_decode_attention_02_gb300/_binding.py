@@ -56,6 +56,9 @@ _SIGS = {
                                   _vp, _vp, ctypes.c_size_t, _vp]),
     "mla_decode_timed": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_float,
                                         _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
+    "mla_decode_diag": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_float,
+                                       _vp, _vp, _vp, ctypes.c_size_t, _vp, ctypes.c_uint64,
+                                       ctypes.c_uint32]),
     "mla_decode_noalloc": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
                                           ctypes.c_float, _vp, _vp, _vp]),
     "mla_decode_check": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
@@ -185,6 +188,25 @@ def decode(p: Plan, q_latent, q_rope, kv_cache, block_table, *, scale: float = D
     main kernel, between the main kernel and the merge, and after the merge
     (``mla_decode_timed``).
     """
+    return _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, None)
+
+
+MLA_INJECT_WITHHOLD_K_LOAD = 0x1
+
+
+def decode_diag(p: Plan, q_latent, q_rope, kv_cache, block_table, *, wait_limit_ns: int,
+                inject: int = 0, scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None):
+    """``mla_decode_diag``: decode with a chosen wait limit and an optional injected stall.
+
+    With inject=MLA_INJECT_WITHHOLD_K_LOAD one K-stage load of the unit that runs the
+    schedule's first item is never issued, so the kernel's bounded waits run out: check(p) then reports
+    MLA_DEV_TIMEOUT and the rows of that unit are unspecified.
+    """
+    return _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, None,
+                   (int(wait_limit_ns), int(inject)))
+
+
+def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, diag):
     import torch
     dev = p.workspace.device
     B, S = p.batch, p.s_q
@@ -205,7 +227,9 @@ def decode(p: Plan, q_latent, q_rope, kv_cache, block_table, *, scale: float = D
             kv_cache.shape[0], block_table.data_ptr(), float(scale), out.data_ptr(),
             lse.data_ptr(), p.workspace.data_ptr(), p.workspace.numel(), _stream_handle(stream)]
     with torch.cuda.device(dev):
-        if events is None:
+        if diag is not None:
+            _check(load_library().mla_decode_diag(*args, *diag), "mla_decode_diag")
+        elif events is None:
             _check(load_library().mla_decode(*args), "mla_decode")
         else:
             if len(events) != 3:

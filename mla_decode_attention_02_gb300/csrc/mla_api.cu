@@ -192,6 +192,17 @@ mla_status mla_decode_timed(const mla_problem *prob, const void *q_latent, const
                        lse, workspace, workspace_bytes, stream, events);
 }
 
+mla_status mla_decode_diag(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                           const void *kv_cache, int64_t num_pages, const int32_t *block_table,
+                           float scale, void *o_latent, float *lse, void *workspace,
+                           size_t workspace_bytes, mla_stream_t stream, uint64_t wait_limit_ns,
+                           uint32_t inject) {
+    if (wait_limit_ns < 1000ull || wait_limit_ns > 60000000000ull) return MLA_ERR_INVALID_ARG;
+    if (inject & ~MLA_INJECT_WITHHOLD_K_LOAD) return MLA_ERR_INVALID_ARG;
+    return decode_impl(prob, q_latent, q_rope, kv_cache, num_pages, block_table, scale, o_latent,
+                       lse, workspace, workspace_bytes, stream, nullptr, wait_limit_ns, inject);
+}
+
 mla_status mla_decode_check(const void *workspace, int32_t *device_status, mla_stream_t stream) {
     if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

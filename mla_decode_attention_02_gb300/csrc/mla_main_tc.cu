@@ -475,7 +475,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         // (both token halves of this CTA's output dims).  Out-of-pool page
         // indices read zeros (TMA bounds fill); the merge warps flag the row.
         const bool kring = warp == 0;
-        const bool withhold = kring && (P.test_flags & 1u) && unit == 0 && rank == 0;   // test hook
+        // injected stall (mla_decode_diag): rank 0 of the unit that runs the schedule's
+        // first item never loads its second K stage
+        const bool withhold = kring && (P.test_flags & MLA_INJECT_WITHHOLD_K_LOAD) && i_begin == 0 &&
+                              i_end > 0 && rank == 0;
         uint32_t g = 0, issued = 0;
         int q_stage_par = -1, q_tile_par = -1;   // parity of the last q copies issued
         bool ok = true;

@@ -117,10 +117,12 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
 
 
 def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
-    """mla_decode_plan, mla_decode, mla_decode_timed and mla_decode_noalloc refuse null or
-    unaligned pointers, an empty page pool, a non-positive or non-finite scale and a workspace
-    below the size any device could need, before they make a CUDA call (so these run without
-    a GPU; a call that passed validation would stop at the first CUDA call instead)."""
+    """mla_decode_plan, mla_decode, mla_decode_timed, mla_decode_diag and mla_decode_noalloc
+    refuse null or unaligned pointers, an empty page pool, a non-positive or non-finite scale
+    and a workspace below the size any device could need (mla_decode_diag also a wait limit
+    outside [1 us, 60 s] and unknown injection bits), before they make a CUDA call (so these
+    run without a GPU; a call that passed validation would stop at the first CUDA call
+    instead)."""
     import mla_decode_attention_02_gb300 as m
     lib = m.load_library()
     A = 0x10000
@@ -131,10 +133,12 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
         return lib.mla_decode_plan(ctypes.byref(prob) if prob is not None else None, seq, ws, nbytes, None)
 
     def decode(prob=good, ptrs=(A, A, A), num_pages=8, bt=A, scale=0.072, out=(A, A), ws=A,
-               nbytes=big, timed=False):
+               nbytes=big, timed="plain", limit=10**6, inject=0):
         args = [ctypes.byref(prob) if prob is not None else None, *ptrs, num_pages, bt, scale, *out, ws,
                 nbytes, None]
-        return lib.mla_decode_timed(*args, None) if timed else lib.mla_decode(*args)
+        if timed == "diag":
+            return lib.mla_decode_diag(*args, limit, inject)
+        return lib.mla_decode_timed(*args, None) if timed == "timed" else lib.mla_decode(*args)
 
     def noalloc(prob=good, ptrs=(A, A, A), num_pages=8, bt=A, seq=A, scale=0.072, out=(A, A)):
         return lib.mla_decode_noalloc(ctypes.byref(prob) if prob is not None else None, *ptrs,
@@ -147,7 +151,7 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
     assert plan(ws=None) == 1
     assert plan(ws=A + 8) == 1
     assert plan(nbytes=64) == 3
-    for timed in (False, True):
+    for timed in ("plain", "timed", "diag"):
         assert decode(prob=None, timed=timed) == 1
         assert decode(prob=_prob(heads=64), timed=timed) == 2
         assert decode(ptrs=(None, A, A), timed=timed) == 1
@@ -163,6 +167,11 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
         for bad in (0.0, -0.072, float("nan"), float("inf"), float("-inf")):
             assert decode(scale=bad, timed=timed) == 1, bad
         assert decode(nbytes=1024, timed=timed) == 3
+    # the diagnostic entry point also bounds its wait limit and knows one injection bit
+    for limit in (0, 999, 60 * 10**9 + 1, 2**64 - 1):
+        assert decode(timed="diag", limit=limit) == 1, limit
+    for inject in (2, 0x80000000, 0xFFFFFFFF):
+        assert decode(timed="diag", inject=inject) == 1, inject
     assert noalloc(prob=None) == 1
     assert noalloc(seq=None) == 1
     assert noalloc(seq=A + 4) == 1
