@@ -14,11 +14,11 @@
 // tokens [32c, 32c + 32) of every 64-token page.
 //
 //   S_c = q . k_c^T     tcgen05 M=128 (heads) N=32 (own tokens) K=576, fp32
-//                       in TMEM; q dims 0-447 are the A operand in TMEM,
-//                       448-575 in shared memory
+//                       in TMEM (two buffers: page parity); q dims 0-383
+//                       are the A operand in TMEM, 384-575 in shared memory
 //   P_c = exp2(S_c*scale*log2e - m)   fp32, rounded to bf16, into this CTA's
-//                       P slot; one bulk copy (issued by a merge warp) puts
-//                       it into the peer's (9 KB per page)
+//                       P slot and, by asynchronous remote stores, into the
+//                       peer's (9 KB per page)
 //   merge: the pair agrees on the running max per head (each side's max
 //          travels with its P half; the lower half is scaled) and rescales
 //          O when the max grows; each half's running row sum rides along
@@ -29,33 +29,31 @@
 // CTA's 32 tokens of a page, all 576 dims, 36 KB) is freed by the score
 // MMAs; the V ring (the page's 64 tokens of this CTA's 256 output dims,
 // 32 KB; own tokens loaded a second time, from L2) and the P ring (the two
-// halves' P tiles and messages, 18 KB, three slots) are freed by PV.  Each
+// halves' P tiles and messages, 18 KB, two slots) are freed by PV.  Each
 // K and V stage is one TMA box of a blocked view of the cache (one SM takes
 // in a few large TMA copies from L2 far faster than many 4 KB ones: about
 // 117 ns per copy plus 5 ns per KB, measured on this part).
 //
-// The P half goes to the peer as one asynchronous bulk copy (9 KB per
-// page), issued by merge warp 8 as soon as the softmax is done with the page:
-// while it waits for the peer's half of a page, it polls the softmax's
-// barriers of the next pages without blocking.  The copy runs on the same
-// engine as the page loads and arrives about 1 us after issue; the three P
-// slots cover that.  The copy's only completion signal is the receiver's
-// mbarrier, so the receiver counts the halves it got into a word of the
-// sender's shared memory; the sender checks that count before it rescales
-// its own half in place (only when the pair's max rose above the half's own:
-// the first pages of an item).  The count is a relaxed store: the copy has
-// finished reading its source before the receiver can see it complete, the
-// store follows that observation and the in-place writes follow the load
-// that sees the store, so the order holds without a release, which would
-// cost about 0.4 us on every page.
+// Each softmax thread stores its head's P row and (max, row sum) twice: into
+// this CTA's P slot and, with st.async, into the peer's, whose mbarrier
+// counts the bytes (one phase per page, armed by a merge warp of the
+// receiver).  The P slot lives from the softmax of a page to the PV of both
+// CTAs, and only a few fit in shared memory, so the exchange latency bounds the
+// page rate: a bulk copy of the half through the TMA engine queued behind the
+// page loads and took about 2 us; the remote stores take about 0.5 us, so two
+// slots suffice and the space of a third holds the second score buffer's q
+// dims instead.  With one score buffer the next page's score MMAs waited for
+// the softmax to read the scores, and that loop (about 1.3 us) set the page
+// rate.
+// The sender's own half stays its own: the merge may rescale it in place.
 //
-// TMEM (512 columns): O half [0,256), S [256,288), q [288,512).  Warp roles
+// TMEM (512 columns): O half [0,256), S [256,320), q [320,512).  Warp roles
 // per CTA: warp 0 loads the K ring and q, warp 2 the V ring; warp 1 issues
 // the score MMAs and warp 3 the PV MMAs (each a whole warp that waits
 // together and issues from one elected lane: about 15 ns per tcgen05.mma,
 // against 35 ns from a lane-0 branch); warps 4-7 (one per TMEM lane quarter,
-// one thread per head) load q into TMEM and compute P; warps 8-11 send P,
-// merge the two halves and run the epilogue.  The score buffer is released
+// one thread per head) load q into TMEM, compute P and send it to the peer;
+// warps 8-11 merge the two halves and run the epilogue.  The score buffer is released
 // right after the softmax's TMEM load, so the next page's score MMAs wait
 // only for that.  Every wait is bounded: on time-out the kernel records
 // MLA_DEV_TIMEOUT and winds down instead of hanging.
@@ -82,7 +80,7 @@ constexpr int kSoftmaxWarp0 = 4;    // warps 4-7
 constexpr int kMergeWarp0 = 8;      // warps 8-11
 constexpr int kKStages = 2;         // K ring (page parity)
 constexpr int kVStages = 2;         // V ring (page parity)
-constexpr int kPSlots = 3;          // P ring (page mod 3)
+constexpr int kPSlots = 2;          // P ring (page parity)
 constexpr int kPrefetch = 3;        // L2 prefetch distance in pages
 constexpr int kClusterSize = 2;
 constexpr int kHalfTok = 32;                      // tokens of a page per CTA
@@ -97,8 +95,9 @@ constexpr uint32_t kPPart = kPHalf + 1024;        // a CTA's part of a P slot: i
 constexpr uint32_t kPSlotBytes = 2 * kPPart;
 static_assert(kPPart % 512 == 0, "64-byte-swizzle tiles start on 512-byte boundaries");
 constexpr uint32_t kQBlk = 128 * 128;             // q block: 128 heads x 64 dims
-constexpr int kQTDims = 448;                      // q dims 0-447 live in TMEM
-constexpr uint32_t kQSBytes = 2 * kQBlk;          // q dims 448-575 in shared memory
+constexpr int kQTDims = 384;                      // q dims 0-383 live in TMEM
+constexpr int kQSBlocks = (kDl + kDr - kQTDims) / 64;   // q dims 384-575: 64-dim blocks in shared memory
+constexpr uint32_t kQSBytes = kQSBlocks * kQBlk;
 constexpr int kRefLag = 4;          // the softmax of page g starts from the agreed max of page g - 4
 constexpr uint32_t kOffQS = 0;
 constexpr uint32_t kOffK = kQSBytes;
@@ -115,8 +114,8 @@ constexpr uint32_t kMsgBytes = kPPart;            // per page: P half tile + (ma
 
 // TMEM columns
 constexpr uint32_t kColO = 0;       // 256 fp32 output columns of this CTA's half
-constexpr uint32_t kColS = 256;     // 32 fp32 scores
-constexpr uint32_t kColQ = 288;     // 224 columns of packed bf16 q (dims 0-447)
+constexpr uint32_t kColS = 256;     // 2 x 32 fp32 scores (page parity)
+constexpr uint32_t kColQ = 320;     // 192 columns of packed bf16 q (dims 0-383)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColQ + kQTDims / 2 == kTmemCols, "TMEM budget");
 
@@ -124,7 +123,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: raise the max only whe
 
 // barrier slots (8 bytes each) in the barrier area
 enum : uint32_t {
-    B_Q_FULL = 0,                        // softmax warps: q dims 0-447 in TMEM
+    B_Q_FULL = 0,                        // softmax warps: q dims 0-383 in TMEM
     B_Q_EMPTY = 1,                       // this CTA's score MMAs done with the item's q
     B_KFULL = 2,                         // + page parity: K stage landed (+tx)
     B_KEMPTY = B_KFULL + 2,              // + page parity: score MMAs done with the K stage
@@ -132,10 +131,10 @@ enum : uint32_t {
     B_VEMPTY = B_VFULL + 2,              // + page parity: PV done with the V stage
     B_PEMPTY = B_VEMPTY + 2,             // + slot: this CTA's PV done with the P slot
     B_PEMPTY_PEER = B_PEMPTY + kPSlots,  // + slot: the peer's PV done with its P slot
-    B_SFULL = B_PEMPTY_PEER + kPSlots,   // scores in TMEM
-    B_SEMPTY = B_SFULL + 1,              // scores read into registers
-    B_SDONE = B_SEMPTY + 1,              // + slot: own P half written
-    B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx)
+    B_SFULL = B_PEMPTY_PEER + kPSlots,   // + page parity: scores in TMEM
+    B_SEMPTY = B_SFULL + 2,              // + page parity: scores read into registers
+    B_SDONE = B_SEMPTY + 2,              // + slot: own P half written
+    B_PMSG = B_SDONE + kPSlots,          // + slot: the peer's P half arrived (+tx, remote stores)
     B_PREADY = B_PMSG + kPSlots,         // + slot: P tile final, PV may run
     B_RESDONE = B_PREADY + kPSlots,      // + page mod kRefLag: agreed max published
     B_PVDONE = B_RESDONE + kRefLag,      // + page parity: PV done
@@ -145,11 +144,10 @@ enum : uint32_t {
     B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
     B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx)
     B_QCOPIED = B_QSTAGE + 1,            // item start: softmax warps moved the staged q to TMEM
-    B_QTILE = B_QCOPIED + 1,             // q dims 448-575 landed in the shared-memory q tile (+tx)
+    B_QTILE = B_QCOPIED + 1,             // q dims 384-575 landed in the shared-memory q tile (+tx)
     B_COUNT = B_QTILE + 1,
 };
-static_assert(B_COUNT * 8 <= 504, "barrier area");
-constexpr uint32_t kOffPeerGot = 504;   // in the barrier area: this CTA's halves the peer has received
+static_assert(B_COUNT * 8 <= 512, "barrier area");
 
 struct Params {
     CUtensorMap tm_q_lat;   // q_latent as [rows*128][512], box 64 x 128, SW128
@@ -188,7 +186,7 @@ __device__ __forceinline__ void fail(const Ctl &c) {
 }
 
 // How a wait acquires: CTA scope; cluster scope, for phases that the peer
-// CTA completes with data (its bulk copies, TMA multicast, its MMAs'
+// CTA completes with data (its remote stores, its MMAs'
 // commits); or not at all, for pure progress signals from the peer.
 enum Scope : int { kCta = 0, kCluster = 1, kSignal = 2 };
 
@@ -231,67 +229,11 @@ __device__ __forceinline__ void wait_landed(const Ctl &c, uint32_t b, uint32_t p
     }
 }
 
-// Bounded wait until a word that the peer writes (release store) reaches `target`.
-__device__ __forceinline__ bool wait_count(const Ctl &c, uint32_t addr, uint32_t target) {
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        if (__all_sync(0xffffffffu, ld_relaxed_local(addr) >= target)) return true;
-        if ((i & 63) == 63) {
-            if (__any_sync(0xffffffffu, *c.abort != 0)) return false;
-            const uint64_t t = globaltimer_ns();
-            if (t0 == 0) {
-                t0 = t;
-            } else if (t - t0 > c.limit_ns) {
-                fail(c);
-                return false;
-            }
-        }
-    }
-}
-
 // Warp-uniform version: every lane waits (and acquires), and the warp agrees
 // on the outcome, so no lane leaves a .sync.aligned sequence early.
 __device__ __forceinline__ bool wait_warp(const Ctl &c, uint32_t b, uint32_t parity,
                                           int scope = kCta) {
     return __all_sync(0xffffffffu, wait(c, b, parity, scope));
-}
-
-// Merge warp 8: wait for the peer's P half of page gp, and meanwhile send this
-// CTA's halves of pages sent .. gp + kPSlots - 1 whose softmax is done.  A send
-// arms this CTA's receive barrier of that page (its phase cannot complete
-// before) and bulk-copies the half and the messages into the peer's slot.
-__device__ bool send_and_wait(const Ctl &c, uint32_t s_p, uint32_t rank, uint32_t peer,
-                              uint32_t &sent, uint32_t total_pages, uint32_t gp) {
-    const uint32_t ps = gp % kPSlots, pu = gp / kPSlots;
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        if (sent < total_pages && sent <= gp + kPSlots - 1 &&
-            __all_sync(0xffffffffu, mbar_test_wait(bar(c, B_SDONE + sent % kPSlots), (sent / kPSlots) & 1))) {
-            if (elect_one()) {
-                const uint32_t s_pst = s_p + (sent % kPSlots) * kPSlotBytes;
-                const uint32_t pmsg = bar(c, B_PMSG + sent % kPSlots);
-                const uint32_t pmsg_peer = mapa(pmsg, peer);
-                mbar_arrive_expect_tx(pmsg, kMsgBytes);
-                bulk_copy_s2c(mapa(s_pst + rank * kPPart, peer), s_pst + rank * kPPart, kPPart, pmsg_peer);
-            }
-            __syncwarp();
-            ++sent;
-            continue;
-        }
-        if (sent > gp && __all_sync(0xffffffffu, mbar_test_wait_cluster(bar(c, B_PMSG + ps), pu & 1)))
-            return true;
-        if ((i & 255) == 255) {
-            if (__any_sync(0xffffffffu, *c.abort != 0)) return false;
-            const uint64_t t = globaltimer_ns();
-            if (t0 == 0) {
-                t0 = t;
-            } else if (t - t0 > c.limit_ns) {
-                if (elect_one()) fail(c);
-                __syncwarp();
-                return false;
-            }
-        }
-    }
 }
 
 // Zero the latent rows of tokens [valid, 64) of a landed V stage (the four
@@ -349,7 +291,7 @@ __device__ __forceinline__ void scale_p_row(uint8_t *tile, int h, float f) {
 // K stage that the item's second page will use (its first page loads into the
 // other one meanwhile), 2-3 in the shared-memory q tile (free once this CTA's
 // score MMAs of the previous item are done).  Loading q through registers costs one L1 wavefront per head
-// row per instruction, so only dims 256-447 take that path, overlapped.
+// row per instruction, so only dims 256-383 take that path, overlapped.
 constexpr int kQStaged = 4;
 __device__ __forceinline__ uint32_t q_stage_off(int b, uint32_t kstage) {
     return b < 2 ? kOffK + kstage * kKStageBytes + b * kQBlk : kOffQS + (b - 2) * kQBlk;
@@ -403,7 +345,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        *reinterpret_cast<volatile uint32_t *>(smem + kOffBar + kOffPeerGot) = 0;
         mbar_init(bar(ctl, B_Q_FULL), 4);
         mbar_init(bar(ctl, B_QTILE), 1);
         mbar_init(bar(ctl, B_QSTAGE), 1);
@@ -423,8 +364,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             mbar_init(bar(ctl, B_PMSG + s), 1);
             mbar_init(bar(ctl, B_PREADY + s), 4);
         }
-        mbar_init(bar(ctl, B_SFULL), 1);
-        mbar_init(bar(ctl, B_SEMPTY), 4);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bar(ctl, B_SFULL + p), 1);
+            mbar_init(bar(ctl, B_SEMPTY + p), 4);
+        }
         for (int r = 0; r < kRefLag; ++r) mbar_init(bar(ctl, B_RESDONE + r), 4);
         mbar_init(bar(ctl, B_PVLAST), 1);
         mbar_init(bar(ctl, B_OFREE), 4);
@@ -503,7 +446,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             // done, so the K stage of this item's second page and the
                             // shared-memory q tile are free.  Stage q dims 0-255 there
                             // (see q_stage_off) beside this page's K load; this item's
-                            // q dims 448-575 follow once the softmax warps moved the
+                            // q dims 384-575 follow once the softmax warps moved the
                             // staged blocks into TMEM.
                             if (ii > 0 && !wait_warp(ctl, bar(ctl, B_Q_EMPTY), (ii - 1) & 1)) {
                                 ok = false;
@@ -539,8 +482,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                                 const uint32_t fb = bar(ctl, B_QTILE);
                                 mbar_arrive_expect_tx(fb, kQSBytes);
                                 const int y = it.row * kHeads;
-                                tma_load_2d(s_qs, &P.tm_q_lat, kQTDims, y, fb);
-                                tma_load_2d(s_qs + kQBlk, &P.tm_q_rope, 0, y, fb);
+                                for (int b = 0; b < kQSBlocks; ++b) {
+                                    const int dim = kQTDims + 64 * b;
+                                    if (dim < kDl) tma_load_2d(s_qs + b * kQBlk, &P.tm_q_lat, dim, y, fb);
+                                    else tma_load_2d(s_qs + b * kQBlk, &P.tm_q_rope, dim - kDl, y, fb);
+                                }
                                 q_tile_par = (int)(ii & 1);
                                 // warm L2 for the next item's q
                                 if (i + 1 < i_end) {
@@ -605,27 +551,29 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             for (int k = 0; k < n && ok; ++k, ++g) {
                 const uint32_t p = g & 1;
                 if (qk) {
-                    // S = q . k_own^T into the single score buffer, once the softmax
-                    // has read the previous page's scores
+                    // S = q . k_own^T into the score buffer of the page's parity, once
+                    // the softmax has read the scores of page g - 2 from it
                     const uint32_t ko = p * kKStageBytes;
+                    const uint32_t tSp = tS + kHalfTok * p;
                     if (!wait_warp(ctl, bar(ctl, B_KFULL + p), (g >> 1) & 1)) { ok = false; break; }
-                    if (g >= 1 && !wait_warp(ctl, bar(ctl, B_SEMPTY), (g - 1) & 1)) {
+                    if (g >= 2 && !wait_warp(ctl, bar(ctl, B_SEMPTY + p), ((g >> 1) - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (elect_one()) {
+                        constexpr int kTs = kQTDims / 16;   // k-steps with q in TMEM
 #pragma unroll
-                        for (int ks = 0; ks < 28; ++ks)
-                            mma_ts(tS, tQ + 8 * ks,
+                        for (int ks = 0; ks < kTs; ++ks)
+                            mma_ts(tSp, tQ + 8 * ks,
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, ks > 0 ? 1u : 0u);
 #pragma unroll
-                        for (int ks = 28; ks < 36; ++ks)
-                            mma_ss(tS, d_qs + (uint64_t)((((ks - 28) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
+                        for (int ks = kTs; ks < 36; ++ks)
+                            mma_ss(tSp, d_qs + (uint64_t)((((ks - kTs) >> 2) * kQBlk + (ks & 3) * 32) >> 4),
                                    d_k + (uint64_t)((ko + (ks >> 2) * kBox + (ks & 3) * 32) >> 4),
                                    id_qk, 1u);
-                        mma_commit(bar(ctl, B_SFULL));
+                        mma_commit(bar(ctl, B_SFULL + p));
                         mma_commit(bar(ctl, B_KEMPTY + p));
                     }
                     __syncwarp();
@@ -700,13 +648,14 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
             // q of this head -> TMEM: dims 0-255 from the staged blocks (the
             // staging was issued after the previous item's score MMAs were done, into
-            // the K stage of the item's second page), dims 256-447 through registers
+            // the K stage of the item's second page), dims 256-383 through registers
             {
+                constexpr int kRegChunks = kQTDims / 64 - kQStaged;
                 const uint4 *src = reinterpret_cast<const uint4 *>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl) +
                                    kQStaged * 8;
-                uint4 x[24];
+                uint4 x[8 * kRegChunks];
 #pragma unroll
-                for (int v = 0; v < 24; ++v) x[v] = src[v];
+                for (int v = 0; v < 8 * kRegChunks; ++v) x[v] = src[v];
                 if (!wait_warp(ctl, bar(ctl, B_QSTAGE), ii & 1)) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -715,7 +664,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_QCOPIED));
 #pragma unroll
-                for (int c = 0; c < 3; ++c) {
+                for (int c = 0; c < kRegChunks; ++c) {
                     uint32_t q[32];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
@@ -749,15 +698,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     }
                     if (k >= kRefLag) base = fmaxf(base, oref[slot * 128 + h]);
                 }
-                if (!wait_warp(ctl, bar(ctl, B_SFULL), g & 1)) { ok = false; break; }
+                const uint32_t sp = g & 1;
+                if (!wait_warp(ctl, bar(ctl, B_SFULL + sp), (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kColS, r);
+                tmem_ld32(tmem + lane_off + kColS + kHalfTok * sp, r);
                 tmem_wait_ld();
-                // the scores are in registers: the next page's score MMAs may start
+                // the scores are in registers: the score MMAs of page g + 2 may start
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(ctl, B_SEMPTY));
+                if (lane == 0) mbar_arrive(bar(ctl, B_SEMPTY + sp));
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
                 const int v_own = min(max(valid - tok_own, 0), kHalfTok);
@@ -799,14 +749,20 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     ok = false;
                     break;
                 }
-                // this half's P row and (max, row sum) -> this CTA's P slot; one bulk
-                // copy (issued by a merge warp) sends them on into the peer's
+                // this half's P row and (max, row sum) -> this CTA's P slot, and the
+                // same bytes into the peer's (its P slot is free: waited above)
                 uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
+                const uint32_t part = ps * kPSlotBytes + rank * kPPart;
+                const uint32_t peer_part = mapa(s_p + part, peer);
+                const uint32_t peer_msg = mapa(bar(ctl, B_PMSG + ps), peer);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(pst + rank * kPPart + p_chunk(h, cc)) =
-                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 v = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    *reinterpret_cast<uint4 *>(pst + rank * kPPart + p_chunk(h, cc)) = v;
+                    st_async_v4(peer_part + p_chunk(h, cc), v, peer_msg);
+                }
                 *reinterpret_cast<float2 *>(pst + rank * kPPart + kPHalf + h * 8) = make_float2(m_used, l_own);
+                st_async_v2f(peer_part + kPHalf + h * 8, m_used, l_own, peer_msg);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + ps));
@@ -821,8 +777,9 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         const float NEG_INF = -INFINITY;
         uint32_t g = 0;
         bool ok = true;
-        // warp 8 sends this CTA's P halves: the next page to send and the unit's page count
-        uint32_t sent = 0, total_pages = 0;
+        // warp 8 arms the receive barrier of each page (armed: pages armed so far;
+        // merged: pages merged so far)
+        uint32_t armed = 0, merged = 0, total_pages = 0;
         for (int i = i_begin; i < i_end; ++i)
             total_pages += (uint32_t)((items[i].kv_end - items[i].kv_begin + kPage - 1) / kPage);
         for (int i = i_begin; i < i_end && ok; ++i) {
@@ -830,7 +787,6 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int b = it.row / P.s_q;
             const int p0 = it.kv_begin / kPage;
             const int n = (it.kv_end - it.kv_begin + kPage - 1) / kPage;
-            const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
             // every page of the item must lie in the pool
             bool bad = false;
@@ -838,8 +794,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 int pg = k0 + lane < n ? P.block_table[(size_t)b * P.max_pages + p0 + k0 + lane] : 0;
                 bad |= __any_sync(0xffffffffu, pg < 0 || (int64_t)pg >= P.num_pages);
             }
-            // Per page: send this CTA's P half on to the peer, then merge the pair's
-            // halves: agree on the max per head (a half computed against a lower
+            // Per page, once both halves are in the slot, merge them: agree on the
+            // max per head (a half computed against a lower
             // one is scaled; O is rescaled when the agreed max grows), publish it
             // for the softmax kRefLag pages on and release the P slot to the PV
             // warp.  Each half's message carries its running row sum, so the sums
@@ -847,32 +803,23 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             float m_ref = NEG_INF, l_run = 0.f;
             for (int k = 0; k < n; ++k) {
                 const uint32_t gp = g + k, par = gp & 1, ps = gp % kPSlots, pu = gp / kPSlots;
-                if (!wait_warp(ctl, bar(ctl, B_SDONE + ps), pu & 1)) { ok = false; break; }
-                uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
                 if (warp == kMergeWarp0) {
-                    // While the peer's half of this page is on its way, send this CTA's
-                    // halves of the pages the softmax has finished (up to kPSlots - 1
-                    // pages ahead), each as soon as it is ready.
-                    if (!send_and_wait(ctl, s_p, rank, peer, sent, total_pages, gp)) { ok = false; break; }
-                    // the peer's half of this page has landed: its copy out of the peer's
-                    // shared memory is complete (the peer may rescale that half in place)
-                    if (elect_one()) st_relaxed_remote(mapa(s_base + kOffBar + kOffPeerGot, peer), gp + 1);
+                    // this page's receive phase: its previous phase (page gp - kPSlots)
+                    // completed before this warp merged that page; bytes that land
+                    // before the arming are counted against it
+                    if (elect_one()) mbar_arrive_expect_tx(bar(ctl, B_PMSG + ps), kMsgBytes);
                     __syncwarp();
-                } else if (!wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) {
+                    armed = gp + 1;
+                }
+                if (!wait_warp(ctl, bar(ctl, B_SDONE + ps), pu & 1) ||
+                    !wait_warp(ctl, bar(ctl, B_PMSG + ps), pu & 1, kCluster)) {
                     ok = false;
                     break;
                 }
+                uint8_t *pst = smem + kOffP + ps * kPSlotBytes;
                 const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPHalf + h * 8);
                 const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPPart + kPHalf + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
-                // this CTA's own half (the source of its copy to the peer) may be rescaled
-                // in place only once the peer has received it
-                const float own_m = rank == 0 ? h0.x : h1.x;
-                if (__any_sync(0xffffffffu, own_m != NEG_INF && own_m < nref) &&
-                    !wait_count(ctl, s_base + kOffBar + kOffPeerGot, gp + 1)) {
-                    ok = false;
-                    break;
-                }
                 if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, fast_exp2(h0.x - nref));
                 if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPPart, h, fast_exp2(h1.x - nref));
                 // O is rescaled (rarely) once the previous PV is done
@@ -910,6 +857,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     mbar_arrive(bar(ctl, B_RESDONE + gp % kRefLag));
                     mbar_arrive(bar(ctl, B_PREADY + ps));
                 }
+                merged = gp + 1;
             }
             g += n;
             if (!ok) break;
@@ -1000,20 +948,24 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 if (lane == 0) mbar_arrive(bar(ctl, B_VEMPTY + p_last));
             }
         }
-        // after a time-out, the halves already sent have been received (their copies
-        // out of this CTA's shared memory are complete) before the CTA may exit
+        // After a time-out, the peer may have stored halves of up to kPSlots pages
+        // past the last one merged here (its softmax waits for this CTA's PV of
+        // page g - kPSlots before it stores page g): wait (bounded) until those
+        // that were sent have landed, so that no remote store reaches this CTA's
+        // shared memory after it exits.
         if (warp == kMergeWarp0 && __any_sync(0xffffffffu, *ctl.abort != 0)) {
             if (lane == 0) {
-                const uint64_t t0 = globaltimer_ns();
-                while (ld_relaxed_local(s_base + kOffBar + kOffPeerGot) < sent &&
-                       globaltimer_ns() - t0 < ctl.limit_ns) {
+                for (uint32_t q = merged; q < merged + kPSlots && q < total_pages; ++q) {
+                    const uint32_t b = bar(ctl, B_PMSG + q % kPSlots);
+                    if (q >= armed) mbar_arrive_expect_tx(b, kMsgBytes);
+                    wait_landed(ctl, b, (q / kPSlots) & 1, kCluster);
                 }
             }
             __syncwarp();
         }
     }
 
-    // teardown: both CTAs finish (every bulk copy acknowledged, no remote arrive in
+    // teardown: both CTAs finish (every remote store landed, no remote arrive in
     // flight) before shared memory and TMEM are released
     tc_fence_before();
     __syncthreads();

@@ -74,20 +74,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// 32-bit relaxed store into another CTA's shared memory and the matching
-// relaxed load of a local word that a peer CTA writes (cluster scope).  A
-// release store at cluster scope waits for every earlier memory operation of
-// the thread; on the per-page path of the main kernel that cost about 0.4 us.
-__device__ __forceinline__ void st_relaxed_remote(uint32_t addr_cluster, uint32_t v) {
-    asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_local(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -209,19 +195,24 @@ __device__ __forceinline__ bool elect_one() {
     return p != 0;
 }
 
-// Bulk copy from this CTA's shared memory to another CTA's (addresses from
-// mapa for the destination and its mbarrier); 16-byte aligned, size a multiple
-// of 16.  Completes `bytes` of the destination mbarrier's transaction count.
-// Its only completion signal is that mbarrier: the bulk async-group waits
-// (cp.async.bulk.wait_group) do not track this form, so the sender learns that
-// its source has been read only from the receiver.
-__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                              uint32_t mbar_cluster) {
+// Asynchronous stores into another CTA's shared memory (addresses from mapa):
+// each completes its bytes on that CTA's mbarrier (transaction count), so the
+// receiver sees them once the barrier's phase completes.  The source is
+// registers, so no buffer of the sender stays in use, and the stores do not
+// queue behind the TMA engine's copies.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint4 v, uint32_t mbar_cluster) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
             dst_cluster),
-        "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar_cluster)
         : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2f(uint32_t dst_cluster, float a, float b, uint32_t mbar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     dst_cluster),
+                 "f"(a), "f"(b), "r"(mbar_cluster)
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 / TMEM
