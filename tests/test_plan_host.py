@@ -11,7 +11,6 @@ import workloads as W
 
 m = pytest.importorskip("mla_decode_attention_02_gb300")
 
-ITEM_COST = 10   # kItemCost of the planner (csrc/mla_internal.h)
 MIN_SPLIT = 8
 
 
@@ -56,11 +55,18 @@ def _check_schedule(seq_lens, s_q, units, max_pages=None):
     assert ub[0] == 0 and ub[-1] == len(items) and np.all(np.diff(ub) >= 0)
     for u in range(units):
         assert np.all(unit[ub[u]:ub[u + 1]] == u)
-    # balance: every unit's load (pages + per-item cost) stays near the target
+    # balance: every unit's load (pages + per-item cost) stays near the target; the
+    # per-item cost (a tuning constant of the planner) follows from the header's total
+    row_pages = [(seq_lens[r // s_q] - s_q + 1 + r % s_q + 63) // 64 for r in range(R)]
+    busy_rows = sum(1 for x in row_pages if x > 0)
+    if h["status"] != 0 or busy_rows == 0:
+        return r, None
+    item_cost = (h["total_cost"] - sum(row_pages)) // busy_rows
+    assert h["total_cost"] == sum(row_pages) + item_cost * busy_rows and item_cost >= 1
     load = np.zeros(units, dtype=np.int64)
     for (row, j0, j1, part), u in zip(items.tolist(), unit.tolist()):
-        load[u] += (j1 - j0 + 63) // 64 + ITEM_COST
-    bound = h["target"] + 2 * (MIN_SPLIT + ITEM_COST)
+        load[u] += (j1 - j0 + 63) // 64 + item_cost
+    bound = h["target"] + 2 * (MIN_SPLIT + item_cost)
     assert load.max() <= bound, (load.max(), h["target"])
     return r, load
 
