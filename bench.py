@@ -63,7 +63,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
-                    help="skip the per_workload lines (mixed, mtp, long, long1m) of the decode stage")
+                    help="skip the per_workload lines (mixed, mtp, long, long1m, and uniform and mixed with "
+                         "power-of-two maxima) of the decode stage")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of from one captured CUDA graph")
     return ap.parse_args()
@@ -323,12 +324,12 @@ def _config(w):
                   f"cache {W.cache_bytes(w.seq_lens) / 1e6:.0f} MB"}
 
 
-PER_WORKLOADS = ("mixed", "mtp", "long", "long1m")
+PER_WORKLOADS = ("mixed", "mtp", "long", "long1m", "uniform+pow2", "mixed+pow2")
 STEP_KERNELS = 3          # launches per step: planner, main kernel, merge
 
 
 def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool, warmup: int,
-             sampler_gpu=None, cpu=None):
+             sampler_gpu=None, cpu=None, pow2_max: bool = False):
     """Time plan + decode of workload `w` on `dev`; returns a dict of times and the inputs.
 
     Two timed regions run the same steps, each step after a 256 MiB L2 flush:
@@ -357,7 +358,7 @@ def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool,
     def step(events=None):
         p = mla.plan(d["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
         mla.decode(p, d["q_latent"], d["q_rope"], d["kv_cache"], d["block_table"],
-                   scale=d["scale"], out=out, lse=lse, events=events)
+                   scale=d["scale"], out=out, lse=lse, events=events, pow2_max=pow2_max)
         return p
 
     for _ in range(max(3, warmup)):
@@ -558,11 +559,14 @@ def run_native(args, rank, world, local):
     per_workload = {}
     if not args.no_per_workload:
         for name in PER_WORKLOADS:
+            # "<workload>+pow2": the same workload with power-of-two running maxima
+            base, _, mode = name.partition("+")
             if name == w.name:
                 continue
-            wk = W.workload(name)
-            r = _measure(wk, dev, world, 20, 0.3, not args.no_graph, 3, sampler_gpu=False)
-            rf = _roofline(wk, r["main_ms"], peaks, peak_src, _ncu_traffic(name))
+            wk = W.workload(base)
+            r = _measure(wk, dev, world, 20, 0.3, not args.no_graph, 3, sampler_gpu=False,
+                         pow2_max=mode == "pow2")
+            rf = _roofline(wk, r["main_ms"], peaks, peak_src, _ncu_traffic(base) if not mode else None)
             kb = W.cache_bytes(wk.seq_lens)
             per_workload[name] = {
                 "config": _config(wk), "steps": r["steps"], "us_per_step": r["step_ms"] * 1e3,

@@ -91,7 +91,8 @@ typedef enum mla_status {
 /*
  * Problem description.  Supported set: batch >= 1, s_q in {1, 2},
  * num_heads == 128, page_size == 64, max_pages_per_seq >= 1,
- * batch * max_pages_per_seq < 2^31, reserved == 0.
+ * batch * max_pages_per_seq < 2^31, flags == 0 or MLA_FLAG_POW2_MAX
+ * (decode entry points only; the prolog and epilog require 0).
  */
 typedef struct mla_problem {
     int32_t batch;
@@ -99,8 +100,18 @@ typedef struct mla_problem {
     int32_t num_heads;
     int32_t page_size;
     int32_t max_pages_per_seq; /* row stride of block_table; bounds every seq_len */
-    int32_t reserved;
+    int32_t flags;
 } mla_problem;
+
+/*
+ * Power-of-two running maxima (the AMLA-style rescale of "Huawei Ascend
+ * servers: DeepSeek V3/R1 inference best practice", section 6.1): the online
+ * softmax keeps each running max as an integer in log2 units (a raised max is
+ * rounded up), so every rescale of P and of the output accumulator is by an
+ * exact power of two.  The result is the same attention (within the usual
+ * tolerance); only the rounding path differs.  The planner ignores the flag.
+ */
+#define MLA_FLAG_POW2_MAX 0x1
 
 /*
  * Bytes of device workspace that mla_decode_plan / mla_decode need for this

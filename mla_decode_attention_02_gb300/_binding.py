@@ -43,7 +43,7 @@ class MLAError(RuntimeError):
 class _Problem(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("s_q", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("max_pages_per_seq", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_pages_per_seq", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER(_Problem)
@@ -107,8 +107,11 @@ def _check(status: int, what: str) -> None:
         raise MLAError(status, what)
 
 
-def _problem(batch: int, s_q: int, max_pages: int) -> _Problem:
-    return _Problem(int(batch), int(s_q), NUM_HEADS, PAGE_SIZE, int(max_pages), 0)
+MLA_FLAG_POW2_MAX = 0x1
+
+
+def _problem(batch: int, s_q: int, max_pages: int, flags: int = 0) -> _Problem:
+    return _Problem(int(batch), int(s_q), NUM_HEADS, PAGE_SIZE, int(max_pages), int(flags))
 
 
 def num_units() -> int:
@@ -157,8 +160,8 @@ class Plan:
     workspace: object   # torch.uint8 CUDA tensor, owned by this Plan
     seq_lens: object    # the device seq_lens it was built from
 
-    def problem(self) -> _Problem:
-        return _problem(self.batch, self.s_q, self.max_pages)
+    def problem(self, flags: int = 0) -> _Problem:
+        return _problem(self.batch, self.s_q, self.max_pages, flags)
 
 
 def plan(seq_lens, *, s_q: int, max_pages_per_seq: int, workspace=None, stream=None) -> Plan:
@@ -181,14 +184,16 @@ def plan(seq_lens, *, s_q: int, max_pages_per_seq: int, workspace=None, stream=N
 
 
 def decode(p: Plan, q_latent, q_rope, kv_cache, block_table, *, scale: float = DEFAULT_SCALE,
-           out=None, lse=None, stream=None, events=None):
+           out=None, lse=None, stream=None, events=None, pow2_max: bool = False):
     """Weight-absorbed MLA decode (``mla_decode``) -> (o_latent bf16, lse fp32).
 
     events: optional three torch.cuda.Event(enable_timing=True) recorded before the
     main kernel, between the main kernel and the merge, and after the merge
-    (``mla_decode_timed``).
+    (``mla_decode_timed``).  pow2_max: power-of-two running maxima
+    (MLA_FLAG_POW2_MAX), so that every rescale is by an exact power of two.
     """
-    return _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, None)
+    return _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, None,
+                   MLA_FLAG_POW2_MAX if pow2_max else 0)
 
 
 MLA_INJECT_WITHHOLD_K_LOAD = 0x1
@@ -203,10 +208,10 @@ def decode_diag(p: Plan, q_latent, q_rope, kv_cache, block_table, *, wait_limit_
     MLA_DEV_TIMEOUT and the rows of that unit are unspecified.
     """
     return _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, None,
-                   (int(wait_limit_ns), int(inject)))
+                   (int(wait_limit_ns), int(inject)), 0)
 
 
-def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, diag):
+def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, diag, flags):
     import torch
     dev = p.workspace.device
     B, S = p.batch, p.s_q
@@ -222,7 +227,7 @@ def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream,
         lse = torch.empty((B, S, NUM_HEADS), dtype=torch.float32, device=dev)
     _req(out, "out", torch.bfloat16, (B, S, NUM_HEADS, D_LATENT), dev)
     _req(lse, "lse", torch.float32, (B, S, NUM_HEADS), dev)
-    prob = p.problem()
+    prob = p.problem(flags)
     args = [ctypes.byref(prob), q_latent.data_ptr(), q_rope.data_ptr(), kv_cache.data_ptr(),
             kv_cache.shape[0], block_table.data_ptr(), float(scale), out.data_ptr(),
             lse.data_ptr(), p.workspace.data_ptr(), p.workspace.numel(), _stream_handle(stream)]

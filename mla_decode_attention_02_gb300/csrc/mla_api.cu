@@ -23,7 +23,7 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
                         int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags,
-                        cudaStream_t stream);
+                        uint32_t flags, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // a bounded device wait gives up after 2 s
 }  // namespace mla
 
@@ -33,7 +33,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 mla_status check_problem(const mla_problem *p) {
     if (!p) return MLA_ERR_INVALID_ARG;
-    if (p->batch < 1 || p->max_pages_per_seq < 1 || p->reserved != 0) return MLA_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->max_pages_per_seq < 1 || (p->flags & ~MLA_FLAG_POW2_MAX) != 0)
+        return MLA_ERR_INVALID_ARG;
     if (p->s_q != 1 && p->s_q != 2) return MLA_ERR_UNSUPPORTED;
     if (p->num_heads != MLA_NUM_HEADS || p->page_size != MLA_PAGE_SIZE) return MLA_ERR_UNSUPPORTED;
     if ((int64_t)p->batch * p->max_pages_per_seq >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
@@ -169,7 +170,8 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
     if (!mark(0)) return MLA_ERR_CUDA;
     cudaError_t e = mla::launch_main(q_latent, q_rope, kv_cache, num_pages, block_table, scale,
                                      workspace, o_latent, lse, prob->batch, prob->s_q,
-                                     prob->max_pages_per_seq, units, wait_limit_ns, test_flags, s);
+                                     prob->max_pages_per_seq, units, wait_limit_ns, test_flags,
+                                     (uint32_t)prob->flags, s);
     if (e != cudaSuccess || !mark(1)) return MLA_ERR_CUDA;
     e = mla::launch_combine(workspace, o_latent, lse, prob->batch, prob->s_q, units, s);
     if (e != cudaSuccess || !mark(2)) return MLA_ERR_CUDA;

@@ -258,7 +258,7 @@ struct LtDescs {
 extern "C" mla_status mla_epilog_uv(const mla_problem *prob, const void *o_latent, const void *w_uv,
                                     void *o_v, int32_t *device_status, mla_stream_t stream) {
     using namespace mla;
-    if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->reserved != 0)
+    if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->flags != 0)
         return MLA_ERR_INVALID_ARG;
     if (prob->s_q != 1 && prob->s_q != 2) return MLA_ERR_UNSUPPORTED;
     if (prob->num_heads != kHeads || prob->page_size != kPage) return MLA_ERR_UNSUPPORTED;

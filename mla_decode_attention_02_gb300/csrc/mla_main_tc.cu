@@ -167,6 +167,7 @@ struct Params {
     float scale_log2;
     int32_t batch, s_q, max_pages, num_units;
     uint32_t test_flags;
+    uint32_t flags;          // mla_problem.flags (MLA_FLAG_POW2_MAX)
 };
 
 struct Ctl {
@@ -197,10 +198,11 @@ __device__ __forceinline__ bool try_wait(uint32_t b, uint32_t parity, int scope)
 }
 
 // Bounded wait for the completion of the phase with the given parity: gives
-// up (and flags the time-out) after kWaitLimitNs, or at once if another
-// thread of the CTA already gave up.
-__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
-                                     int scope = kCta) {
+// up (and flags the time-out) after the limit, or at once if another thread
+// of the CTA already gave up.  The first probe is inline; the polling loop is
+// out of line, so that the many wait sites of the page loop stay small in the
+// instruction cache.
+__device__ __noinline__ bool wait_slow(const Ctl c, uint32_t b, uint32_t parity, int scope) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
         if (try_wait(b, parity, scope)) return true;
@@ -217,9 +219,14 @@ __device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ bool wait(const Ctl &c, uint32_t b, uint32_t parity,
+                                     int scope = kCta) {
+    return try_wait(b, parity, scope) || wait_slow(c, b, parity, scope);
+}
+
 // Teardown wait that ignores the abort flag (for copies already in flight,
-// which always land, and acknowledgements of them): bounded by the limit.
-__device__ __forceinline__ void wait_landed(const Ctl &c, uint32_t b, uint32_t parity, int scope = kCta) {
+// which always land): bounded by the limit.
+__device__ __noinline__ void wait_landed(const Ctl c, uint32_t b, uint32_t parity, int scope = kCta) {
     const uint64_t t0 = globaltimer_ns();
     while (!try_wait(b, parity, scope)) {
         if (globaltimer_ns() - t0 > c.limit_ns) {
@@ -254,6 +261,21 @@ __device__ __noinline__ void zero_v_tail(uint8_t *vst, int valid, int lane) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 2^k for an integer k <= 0, exactly (0 below the normal range).
+__device__ __forceinline__ float pow2i(int k) {
+    return k < -126 ? 0.f : __int_as_float((k + 127) << 23);
+}
+
+// The factor 2^d that moves values from one reference max to a higher one
+// (d <= 0).  With power-of-two maxima (MLA_FLAG_POW2_MAX) every reference is an
+// integer in log2 units, d is an integer and the factor is built exactly from
+// its exponent bits, so rescaling a bf16 P row or the fp32 O accumulator is
+// exact; otherwise it is ex2.approx.
+__device__ __forceinline__ float fast_exp2(float x);
+__device__ __forceinline__ float rescale(float d, bool pow2) {
+    return pow2 ? pow2i((int)d) : fast_exp2(d);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -411,6 +433,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         atomicOr(&hdr->status, MLA_DEV_BAD_PLAN);
     }
     const int tok_own = kHalfTok * (int)rank;
+    const bool pow2 = (P.flags & MLA_FLAG_POW2_MAX) != 0;   // power-of-two running maxima
 
     if (warp == 0 || warp == kVWarp) {
         // ------------------------------------------------------------ TMA producers
@@ -728,8 +751,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 }
                 const float lm = rmax * sc;
                 // raise the max only when this half's page exceeds it by > 2^8
-                const float m_used = (lm - base > kRescaleThreshold) ? lm : base;
-                const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : fast_exp2(m_prev - m_used));
+                // (with power-of-two maxima a raised max is rounded up to an integer, so
+                // that every later rescale is by an exact power of two)
+                const float m_used = (lm - base > kRescaleThreshold) ? (pow2 ? ceilf(lm) : lm) : base;
+                const float l_scale = m_prev == NEG_INF ? 0.f : (m_used == m_prev ? 1.f : rescale(m_prev - m_used, pow2));
                 m_prev = m_used;
                 const float mu = m_used == NEG_INF ? 0.f : m_used;
                 uint32_t pk[16];
@@ -820,8 +845,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 const float2 h0 = *reinterpret_cast<const float2 *>(pst + kPHalf + h * 8);
                 const float2 h1 = *reinterpret_cast<const float2 *>(pst + kPPart + kPHalf + h * 8);
                 const float nref = fmaxf(m_ref, fmaxf(h0.x, h1.x));   // finite: token 0 is valid
-                if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, fast_exp2(h0.x - nref));
-                if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPPart, h, fast_exp2(h1.x - nref));
+                if (h0.x != NEG_INF && h0.x < nref) scale_p_row(pst, h, rescale(h0.x - nref, pow2));
+                if (h1.x != NEG_INF && h1.x < nref) scale_p_row(pst + kPPart, h, rescale(h1.x - nref, pow2));
                 // O is rescaled (rarely) once the previous PV is done
                 const bool need = k > 0 && nref > m_ref;
                 if (__any_sync(0xffffffffu, need)) {
@@ -830,7 +855,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         break;
                     }
                     tc_fence_after();
-                    const float a = need ? fast_exp2(m_ref - nref) : 1.f;
+                    const float a = need ? rescale(m_ref - nref, pow2) : 1.f;
 #pragma unroll 1
                     for (int ch = 0; ch < 8; ++ch) {
                         uint32_t o[32];
@@ -846,8 +871,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 oref[(gp % kRefLag) * 128 + h] = m_ref;
                 if (k == n - 1) {
                     // both halves' row sums, relative to the final max (same order in both CTAs)
-                    const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : fast_exp2(h0.x - nref));
-                    const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : fast_exp2(h1.x - nref));
+                    const float f0 = h0.x == NEG_INF ? 0.f : (h0.x == nref ? 1.f : rescale(h0.x - nref, pow2));
+                    const float f1 = h1.x == NEG_INF ? 0.f : (h1.x == nref ? 1.f : rescale(h1.x - nref, pow2));
                     l_run = h0.y * f0 + h1.y * f1;
                 }
                 fence_proxy_async_smem();
@@ -1059,7 +1084,7 @@ cudaError_t main_units(int32_t *units) {
 cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv,
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
-                        int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags,
+                        int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags, uint32_t flags,
                         cudaStream_t stream) {
     Params p;
     const cuuint64_t qrows = (cuuint64_t)batch * s_q * kHeads;
@@ -1096,6 +1121,7 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     p.num_pages = num_pages;
     p.wait_limit_ns = wait_limit_ns;
     p.test_flags = test_flags;
+    p.flags = flags;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.batch = batch;
     p.s_q = s_q;

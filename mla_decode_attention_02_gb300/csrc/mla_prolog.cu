@@ -395,7 +395,7 @@ extern "C" mla_status mla_prolog(const mla_problem *prob, const void *q_nope, co
                                  const int32_t *seq_lens, void *q_latent, void *q_rope,
                                  int32_t *device_status, mla_stream_t stream) {
     using namespace mla;
-    if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->reserved != 0)
+    if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->flags != 0)
         return MLA_ERR_INVALID_ARG;
     if (prob->s_q != 1 && prob->s_q != 2) return MLA_ERR_UNSUPPORTED;
     if (prob->num_heads != kHeads || prob->page_size != kPage) return MLA_ERR_UNSUPPORTED;

@@ -17,13 +17,13 @@ def to_device(inp, device="cuda"):
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def run_gpu(inp, *, max_pages=None, check_status=True):
+def run_gpu(inp, *, max_pages=None, check_status=True, pow2_max=False):
     """Plan + decode on cuda:0 through the C ABI; returns (o fp64 numpy, lse fp64 numpy, status)."""
     d = to_device(inp)
     mp = d["block_table"].shape[1] if max_pages is None else max_pages
     p = mla.plan(d["seq_lens"], s_q=d["s_q"], max_pages_per_seq=mp)
     o, lse = mla.decode(p, d["q_latent"], d["q_rope"], d["kv_cache"], d["block_table"],
-                        scale=d["scale"])
+                        scale=d["scale"], pow2_max=pow2_max)
     status = mla.check(p)
     if check_status:
         assert status == 0, f"device status {status:#x}"

@@ -68,9 +68,9 @@ def test_missing_library_fails_loudly(tmp_path):
         b._lib = saved
 
 
-def _prob(batch=2, s_q=1, heads=128, page=64, max_pages=4):
+def _prob(batch=2, s_q=1, heads=128, page=64, max_pages=4, flags=0):
     import mla_decode_attention_02_gb300._binding as b
-    return b._Problem(batch, s_q, heads, page, max_pages, 0)
+    return b._Problem(batch, s_q, heads, page, max_pages, flags)
 
 
 def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
@@ -91,6 +91,7 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
     assert prolog(_prob(heads=64)) == 2
     assert prolog(_prob(page=32)) == 2
     assert prolog(_prob(batch=0)) == 1
+    assert prolog(_prob(flags=1)) == 1                                    # decode-only flag
     assert prolog(_prob(batch=1, max_pages=1 << 25)) == 2                 # positions past 2^31
     assert prolog(good, ptrs=[A, A + 8, A, A, A, A]) == 1          # q_pe not 16-byte aligned
     assert prolog(good, eps=-1.0) == 1
@@ -104,6 +105,7 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
 
     assert lib.mla_epilog_uv(None, A, A, A, A, None) == 1
     assert lib.mla_epilog_uv(ctypes.byref(_prob(s_q=3)), A, A, A, A, None) == 2
+    assert lib.mla_epilog_uv(ctypes.byref(_prob(flags=1)), A, A, A, A, None) == 1
     assert lib.mla_epilog_uv(ctypes.byref(good), A, A, None, A, None) == 1
     assert lib.mla_epilog_uv(ctypes.byref(good), A, A, A, None, None) == 1
     assert lib.mla_epilog_oproj(0, 7168, A, A, A, None, 0, None) == 1
@@ -146,6 +148,8 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
 
     assert plan(prob=None) == 1
     assert plan(prob=_prob(s_q=3)) == 2
+    assert plan(prob=_prob(flags=2)) == 1                                 # unknown flag bit
+    assert plan(prob=_prob(flags=1), nbytes=64) == 3                      # the known one passes on
     assert plan(seq=None) == 1
     assert plan(seq=A + 4) == 1
     assert plan(ws=None) == 1
@@ -166,6 +170,8 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
         assert decode(num_pages=1 << 31, timed=timed) == 1
         for bad in (0.0, -0.072, float("nan"), float("inf"), float("-inf")):
             assert decode(scale=bad, timed=timed) == 1, bad
+        assert decode(prob=_prob(flags=-1), timed=timed) == 1
+        assert decode(prob=_prob(flags=1), nbytes=1024, timed=timed) == 3
         assert decode(nbytes=1024, timed=timed) == 3
     # the diagnostic entry point also bounds its wait limit and knows one injection bit
     for limit in (0, 999, 60 * 10**9 + 1, 2**64 - 1):
