@@ -51,21 +51,17 @@ mla_status mla_epilog_uv(const mla_problem *prob, const void *o_latent, const vo
                          void *o_v, int32_t *device_status, mla_stream_t stream);
 
 /*
- * Device workspace the output projection may use (bytes): pass at least this
- * much to mla_epilog_oproj for its fastest algorithms; less (or none) is
- * allowed and only narrows the choice.
- */
-size_t mla_epilog_oproj_workspace_size(void);
-
-/*
  * The output projection: out = o_v . w_o^T, bf16 in and out, fp32
- * accumulation, for `tokens` rows of o_v (viewed as [tokens][16384]).  A
- * plain dense GEMM, run by cuBLASLt on `stream` with the caller's workspace
- * (workspace may be NULL when workspace_bytes is 0).  tokens >= 1;
- * hidden >= 8 and a multiple of 8.
+ * accumulation, for `tokens` rows of o_v (viewed as [tokens][16384]): one
+ * tensor-core kernel on `stream` (each SM pair holds 128 outputs and splits
+ * the 16384-term sums in two halves that it adds in a fixed way, so the
+ * result is the same on every run).  tokens >= 1; hidden >= 8 and a multiple
+ * of 8.  device_status: a device int32 the caller clears; MLA_DEV_TIMEOUT is
+ * OR-ed in if a bounded wait inside the kernel ran out (that tile of out is
+ * then not written).
  */
 mla_status mla_epilog_oproj(int32_t tokens, int32_t hidden, const void *o_v, const void *w_o,
-                            void *out, void *workspace, size_t workspace_bytes, mla_stream_t stream);
+                            void *out, int32_t *device_status, mla_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -70,9 +70,7 @@ _SIGS = {
     "mla_prolog_rope_table": (ctypes.c_int, [ctypes.c_double, _vp, _vp]),
     "mla_epilog_uv": (ctypes.c_int, [_P, _vp, _vp, _vp, _vp, _vp]),
     "mla_cache_quantize_fp8": (ctypes.c_int, [_vp, ctypes.c_int64, _vp, _vp]),
-    "mla_epilog_oproj_workspace_size": (ctypes.c_size_t, []),
-    "mla_epilog_oproj": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp,
-                                        ctypes.c_size_t, _vp]),
+    "mla_epilog_oproj": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -397,11 +395,12 @@ def epilog_uv(o_latent, w_uv, *, o_v=None, status=None, stream=None):
     return o_v, status
 
 
-def epilog_oproj(o_v, w_o, *, out=None, workspace=None, stream=None):
-    """The output projection (``mla_epilog_oproj``, cuBLASLt): out = o_v . W_O^T.
+def epilog_oproj(o_v, w_o, *, out=None, status=None, stream=None):
+    """The output projection (``mla_epilog_oproj``, a tensor-core kernel): out = o_v . W_O^T.
 
     o_v [..][128][128] bf16 viewed as [tokens][16384], w_o [hidden][16384] bf16 ->
-    out [tokens][hidden] bf16.  workspace: optional uint8 device tensor.
+    out [tokens][hidden] bf16.  status: optional int32 device tensor of one element that
+    the call ORs MLA_DEV_TIMEOUT into if a bounded wait in the kernel runs out.
     """
     import torch
     dev = o_v.device
@@ -416,19 +415,14 @@ def epilog_oproj(o_v, w_o, *, out=None, workspace=None, stream=None):
     if out is None:
         out = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
     _req(out, "out", torch.bfloat16, (tokens, hidden), dev)
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        _req(workspace, "workspace", torch.uint8, None, dev)
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _req(status, "status", torch.int32, None, dev)
     with torch.cuda.device(dev):
         _check(load_library().mla_epilog_oproj(int(tokens), int(hidden), o_v.data_ptr(), w_o.data_ptr(),
-                                               out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream)),
+                                               out.data_ptr(), status.data_ptr(), _stream_handle(stream)),
                "mla_epilog_oproj")
     return out
-
-
-def epilog_oproj_workspace_size() -> int:
-    return int(load_library().mla_epilog_oproj_workspace_size())
 
 
 FP8_ROW_BYTES = 656

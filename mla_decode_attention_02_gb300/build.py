@@ -2,9 +2,8 @@
 
 All translation units compile in parallel and link with -shared; the CUDA
 runtime links statically and the driver API is reached through
-cudaGetDriverEntryPoint.  At load time the library needs libc, the NVIDIA
-driver and libcublasLt (the output projection's plain GEMM, found through an
-rpath to the toolkit's lib64).
+cudaGetDriverEntryPoint.  At load time the library needs nothing but libc and
+the NVIDIA driver: every kernel is this library's own.
 """
 
 from __future__ import annotations
@@ -70,10 +69,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple = ()) -
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    # cuBLASLt (the output projection's plain GEMM) is found next to the CUDA runtime
-    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
-    cmd = [nvcc, ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-L", libdir, "-lcublasLt",
-           "-Xlinker", "-rpath=" + libdir]
+    cmd = [nvcc, ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -21,9 +21,7 @@
 //    per thread), round to bf16, stage the tile conflict-free in shared
 //    memory and store each token's 256-byte row contiguously.  With fewer
 //    than 128 tokens the A box holds only round_up(tokens, 8) rows.
-//  - o_proj: a plain dense GEMM (weights 16384 x hidden, bf16, fp32
-//    accumulate), run by cuBLASLt with the caller's workspace.
-#include <cublasLt.h>
+//  - o_proj: its own tensor-core kernel, in mla_oproj.cu.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,9 +29,7 @@
 
 #include <algorithm>
 #include <cstdint>
-#include <map>
 #include <mutex>
-#include <tuple>
 
 #include "mla_epilog.h"
 #include "mla_internal.h"
@@ -220,37 +216,7 @@ __global__ void __launch_bounds__(kThreadsE, 2) mla_epilog_uv_kernel(const __gri
 std::mutex g_mutex;
 bool g_attr[64];
 
-struct LtState {
-    cublasLtHandle_t handle = nullptr;
-    std::map<std::tuple<int32_t, int32_t, size_t>, std::pair<bool, cublasLtMatmulAlgo_t>> algos;
-};
-LtState g_lt[64];
-
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-struct LtDescs {
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
-    ~LtDescs() {
-        if (c) cublasLtMatrixLayoutDestroy(c);
-        if (b) cublasLtMatrixLayoutDestroy(b);
-        if (a) cublasLtMatrixLayoutDestroy(a);
-        if (op) cublasLtMatmulDescDestroy(op);
-    }
-    // column-major view: out^T [hidden x tokens] = (w_o as [16384 x hidden])^T . (o_v as [16384 x tokens])
-    bool make(int32_t tokens, int32_t hidden) {
-        const int64_t K = (int64_t)kHeads * kDv;
-        const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-        return cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
-               cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) ==
-                   CUBLAS_STATUS_SUCCESS &&
-               cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) ==
-                   CUBLAS_STATUS_SUCCESS &&
-               cublasLtMatrixLayoutCreate(&a, CUDA_R_16BF, K, hidden, K) == CUBLAS_STATUS_SUCCESS &&
-               cublasLtMatrixLayoutCreate(&b, CUDA_R_16BF, K, tokens, K) == CUBLAS_STATUS_SUCCESS &&
-               cublasLtMatrixLayoutCreate(&c, CUDA_R_16BF, hidden, tokens, hidden) == CUBLAS_STATUS_SUCCESS;
-    }
-};
 
 }  // namespace
 }  // namespace mla
@@ -305,48 +271,4 @@ extern "C" mla_status mla_epilog_uv(const mla_problem *prob, const void *o_laten
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, mla_epilog_uv_kernel, p) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
-}
-
-extern "C" size_t mla_epilog_oproj_workspace_size(void) { return (size_t)32 << 20; }
-
-extern "C" mla_status mla_epilog_oproj(int32_t tokens, int32_t hidden, const void *o_v, const void *w_o,
-                                       void *out, void *workspace, size_t workspace_bytes,
-                                       mla_stream_t stream) {
-    using namespace mla;
-    if (tokens < 1 || hidden < 8 || hidden % 8 != 0 || !aligned16(o_v) || !aligned16(w_o) ||
-        !aligned16(out) || (workspace_bytes && !aligned16(workspace)))
-        return MLA_ERR_INVALID_ARG;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
-    LtDescs d;
-    if (!d.make(tokens, hidden)) return MLA_ERR_CUDA;
-    cublasLtMatmulAlgo_t algo;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        LtState &st = g_lt[dev];
-        if (!st.handle && cublasLtCreate(&st.handle) != CUBLAS_STATUS_SUCCESS) return MLA_ERR_CUDA;
-        const auto key = std::make_tuple(tokens, hidden, workspace_bytes);
-        auto it = st.algos.find(key);
-        if (it == st.algos.end()) {
-            cublasLtMatmulPreference_t pref = nullptr;
-            cublasLtMatmulHeuristicResult_t res = {};
-            int found = 0;
-            bool ok = cublasLtMatmulPreferenceCreate(&pref) == CUBLAS_STATUS_SUCCESS &&
-                      cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                                           &workspace_bytes, sizeof(workspace_bytes)) ==
-                          CUBLAS_STATUS_SUCCESS &&
-                      cublasLtMatmulAlgoGetHeuristic(st.handle, d.op, d.a, d.b, d.c, d.c, pref, 1, &res,
-                                                     &found) == CUBLAS_STATUS_SUCCESS &&
-                      found > 0;
-            if (pref) cublasLtMatmulPreferenceDestroy(pref);
-            if (!ok) return MLA_ERR_CUDA;
-            it = st.algos.emplace(key, std::make_pair(true, res.algo)).first;
-        }
-        algo = it->second.second;
-    }
-    const float alpha = 1.0f, beta = 0.0f;
-    const cublasStatus_t s =
-        cublasLtMatmul(g_lt[dev].handle, d.op, &alpha, w_o, d.a, o_v, d.b, &beta, out, d.c, out, d.c, &algo,
-                       workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
-    return s == CUBLAS_STATUS_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -108,11 +108,11 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
     assert lib.mla_epilog_uv(ctypes.byref(_prob(flags=1)), A, A, A, A, None) == 1
     assert lib.mla_epilog_uv(ctypes.byref(good), A, A, None, A, None) == 1
     assert lib.mla_epilog_uv(ctypes.byref(good), A, A, A, None, None) == 1
-    assert lib.mla_epilog_oproj(0, 7168, A, A, A, None, 0, None) == 1
-    assert lib.mla_epilog_oproj(4, 7, A, A, A, None, 0, None) == 1
-    assert lib.mla_epilog_oproj(4, 7168, A + 2, A, A, None, 0, None) == 1
-    assert lib.mla_epilog_oproj(4, 7168, A, A, A, None, 1024, None) == 1   # workspace bytes, no pointer
-    assert lib.mla_epilog_oproj_workspace_size() == 32 << 20
+    assert lib.mla_epilog_oproj(0, 7168, A, A, A, A, None) == 1
+    assert lib.mla_epilog_oproj(4, 7, A, A, A, A, None) == 1
+    assert lib.mla_epilog_oproj(4, 7168, A + 2, A, A, A, None) == 1
+    assert lib.mla_epilog_oproj(4, 7168, A, A, A, None, None) == 1         # no status word
+    assert lib.mla_epilog_oproj(4, 7168, A, A, A, A + 2, None) == 1        # misaligned status word
     assert lib.mla_cache_quantize_fp8(None, 64, A, None) == 1
     assert lib.mla_cache_quantize_fp8(A, 0, A, None) == 1
     assert lib.mla_cache_quantize_fp8(A, 64, A + 4, None) == 1

@@ -50,21 +50,38 @@ def test_uv_parity(batch, s_q):
 def test_oproj_parity(tokens, hidden):
     e = W.epilog_tensors(tokens, seed=100 + tokens, hidden=hidden)
     o_v = (e["o_latent"][:, :, :128].contiguous())          # any bf16 [T][128][128] input
-    ws = torch.empty(mla.epilog_oproj_workspace_size(), dtype=torch.uint8, device="cuda")
-    out = mla.epilog_oproj(o_v.cuda(), e["w_o"].cuda(), workspace=ws)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mla.epilog_oproj(o_v.cuda(), e["w_o"].cuda(), status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     ref = E.o_project(o_v, e["w_o"])
     absdot = E.o_project(np.abs(_np(o_v)), np.abs(_np(e["w_o"])))
     _within(_np(out), ref, absdot, 128 * 128, f"out T={tokens} hidden={hidden}")
 
 
-def test_oproj_without_workspace():
-    e = W.epilog_tensors(8, seed=7, hidden=512)
+@pytest.mark.parametrize("tokens,hidden", [(8, 512), (300, 1000), (129, 136)])
+def test_oproj_ragged_shapes(tokens, hidden):
+    """Token counts past one 256-token tile and hidden sizes that end inside a 128-output
+    tile: the rows past the ends read zeros and are not stored."""
+    e = W.epilog_tensors(tokens, seed=7 + tokens, hidden=hidden)
     o_v = e["o_latent"][:, :, :128].contiguous()
-    out = mla.epilog_oproj(o_v.cuda(), e["w_o"].cuda())
+    guard = torch.full((tokens + 2, hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = guard[:tokens]
+    mla.epilog_oproj(o_v.cuda(), e["w_o"].cuda(), out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(guard[tokens:]).all()            # nothing past the last token row
     ref = E.o_project(o_v, e["w_o"])
     absdot = E.o_project(np.abs(_np(o_v)), np.abs(_np(e["w_o"])))
-    _within(_np(out), ref, absdot, 128 * 128, "out without workspace")
+    _within(_np(out), ref, absdot, 128 * 128, f"out T={tokens} hidden={hidden}")
+
+
+def test_oproj_deterministic():
+    e = W.epilog_tensors(256, seed=9, hidden=7168)
+    o_v = e["o_latent"][:, :, :128].contiguous().cuda()
+    w_o = e["w_o"].cuda()
+    a = mla.epilog_oproj(o_v, w_o)
+    b = mla.epilog_oproj(o_v, w_o)
+    assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("s_q", [1, 2])
@@ -112,8 +129,7 @@ def test_epilog_parity_bench_configuration(name):
     T = w.batch * w.s_q
     e = W.epilog_tensors(T, w.seed)
     o_v, st = mla.epilog_uv(e["o_latent"].view(w.batch, w.s_q, 128, 512).cuda(), e["w_uv"].cuda())
-    ws = torch.empty(mla.epilog_oproj_workspace_size(), dtype=torch.uint8, device="cuda")
-    out = mla.epilog_oproj(o_v, e["w_o"].cuda(), workspace=ws)
+    out = mla.epilog_oproj(o_v, e["w_o"].cuda())
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     ref_v = E.uv_project(e["o_latent"], e["w_uv"])
