@@ -292,7 +292,7 @@ __device__ __forceinline__ uint32_t p_chunk(int h, int cc) {
 }
 
 // Scale head h's 32 bf16 values in one P half tile by f.
-__device__ __forceinline__ void scale_p_row(uint8_t *tile, int h, float f) {
+__device__ __noinline__ void scale_p_row(uint8_t *tile, int h, float f) {
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
         uint4 *p = reinterpret_cast<uint4 *>(tile + p_chunk(h, cc));
@@ -336,6 +336,96 @@ __device__ __forceinline__ void q_stage_to_tmem(const uint8_t *smem, int b, uint
         q[4 * c + 3] = x.w;
     }
     tmem_st32(tq + b * 32, q);
+}
+
+// Item epilogue, one merge warp (32 heads): normalise this CTA's output half
+// (the last PV is done), store it as bf16 output rows or fp32 partial rows
+// and the lse, and arrive on OFREE (TMEM read) and EPI (staging done).  The
+// rows go through the last page's V stage (free now: its MMAs are done and it
+// is only refilled after the epilogue releases it), so that every global
+// store writes 256 contiguous bytes of one row.  Out of line: once per item.
+__device__ __noinline__ void item_epilogue(const Ctl ctl, __nv_bfloat16 *o_latent, float *lse_out, float *o_part,
+                                           float *lse_part, PlanHeader *hdr, uint32_t lstage, uint32_t tO,
+                                           const WorkItem it, bool bad, float l_run, float m_ref, int quarter,
+                                           int lane, uint32_t rank) {
+    const int h = quarter * 32 + lane;
+    const float nan = __int_as_float(0x7fc00000);
+    const float inv = bad ? nan : 1.f / l_run;
+    const float lse = bad ? nan : (m_ref + log2f(l_run)) * 0.69314718055994531f;
+    const uint32_t stg = lstage + quarter * 8192;   // 32 rows x 256 B (shared address)
+    const uint32_t my_stg = stg + lane * 256;
+    const bool final_out = it.part < 0;
+    const int passes = final_out ? 2 : 4;     // 256 B of a row per pass
+#pragma unroll 1
+    for (int pass = 0; pass < passes; ++pass) {
+        // TMEM -> normalised values -> swizzled staging row (chunk c at c ^ lane)
+        if (final_out) {
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(tO + (pass * 4 + ch) * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 v;
+                    v.x = pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                    v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                    v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                    v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                    const int c = ch * 4 + q;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(my_stg + ((c ^ (lane & 15)) << 4)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(tO + (pass * 2 + ch) * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = ch * 8 + q;
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(my_stg + ((c ^ (lane & 15)) << 4)),
+                                 "f"(__uint_as_float(o[4 * q]) * inv), "f"(__uint_as_float(o[4 * q + 1]) * inv),
+                                 "f"(__uint_as_float(o[4 * q + 2]) * inv), "f"(__uint_as_float(o[4 * q + 3]) * inv)
+                                 : "memory");
+                }
+            }
+        }
+        if (pass == passes - 1) {  // O fully read: the next item's PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl, B_OFREE));
+        }
+        __syncwarp();
+        // staging -> global: two rows per step, 16 lanes x 16 B contiguous per row
+        const int j = lane & 15;
+#pragma unroll 4
+        for (int st = 0; st < 16; ++st) {
+            const int r = 2 * st + (lane >> 4);
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stg + r * 256 + ((j ^ (r & 15)) << 4)) : "memory");
+            const size_t hr = (size_t)it.row * kHeads + quarter * 32 + r;
+            if (final_out) {
+                reinterpret_cast<uint4 *>(o_latent + hr * kDl + rank * 256 + pass * 128)[j] = v;
+            } else {
+                const size_t slot = (size_t)it.part * kHeads + quarter * 32 + r;
+                reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + pass * 64)[j] = v;
+            }
+        }
+        __syncwarp();
+    }
+    if (rank == 0) {
+        if (final_out) lse_out[(size_t)it.row * kHeads + h] = lse;
+        else lse_part[(size_t)it.part * kHeads + h] = lse;
+    }
+    if (bad && lane == 0 && rank == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
+    // once every merge warp is done with the stage, release it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -894,80 +984,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             if (!wait_warp(ctl, bar(ctl, B_PVLAST), ii & 1)) break;
             tc_fence_after();
             const uint32_t p_last = (g - 1) & 1;
-            uint8_t *lstage = smem + kOffV + p_last * kVStageBytes;
-            const float nan = __int_as_float(0x7fc00000);
-            const float inv = bad ? nan : 1.f / l_run;
-            const float lse = bad ? nan : (m_ref + log2f(l_run)) * 0.69314718055994531f;
-            uint8_t *stg = lstage + quarter * 8192;   // 32 rows x 256 B
-            uint8_t *my_stg = stg + lane * 256;
-            const bool final_out = it.part < 0;
-            const int passes = final_out ? 2 : 4;     // 256 B of a row per pass
-#pragma unroll 1
-            for (int pass = 0; pass < passes; ++pass) {
-                // TMEM -> normalised values -> swizzled staging row (chunk c at c ^ lane)
-                if (final_out) {
-#pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + (pass * 4 + ch) * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                            v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                            v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                            v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                            const int c = ch * 4 + q;
-                            *reinterpret_cast<uint4 *>(my_stg + ((c ^ (lane & 15)) << 4)) = v;
-                        }
-                    }
-                } else {
-#pragma unroll 1
-                    for (int ch = 0; ch < 2; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + (pass * 2 + ch) * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int c = ch * 8 + q;
-                            *reinterpret_cast<float4 *>(my_stg + ((c ^ (lane & 15)) << 4)) =
-                                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
-                        }
-                    }
-                }
-                if (pass == passes - 1) {  // O fully read: the next item's PV may overwrite it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(ctl, B_OFREE));
-                }
-                __syncwarp();
-                // staging -> global: two rows per step, 16 lanes x 16 B contiguous per row
-                const int j = lane & 15;
-#pragma unroll 4
-                for (int st = 0; st < 16; ++st) {
-                    const int r = 2 * st + (lane >> 4);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 256 + ((j ^ (r & 15)) << 4));
-                    const size_t hr = (size_t)it.row * kHeads + quarter * 32 + r;
-                    if (final_out) {
-                        reinterpret_cast<uint4 *>(P.o_latent + hr * kDl + rank * 256 + pass * 128)[j] = v;
-                    } else {
-                        const size_t slot = (size_t)it.part * kHeads + quarter * 32 + r;
-                        reinterpret_cast<uint4 *>(o_part + slot * kDl + rank * 256 + pass * 64)[j] = v;
-                    }
-                }
-                __syncwarp();
-            }
-            if (rank == 0) {
-                if (final_out) P.lse[(size_t)it.row * kHeads + h] = lse;
-                else lse_part[(size_t)it.part * kHeads + h] = lse;
-            }
-            if (bad && lane == 0 && rank == 0) atomicOr(&hdr->status, MLA_DEV_BAD_PAGE);
-            // once every merge warp is done with the stage, release it
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
+            item_epilogue(ctl, P.o_latent, P.lse, o_part, lse_part, hdr, s_base + kOffV + p_last * kVStageBytes, tO,
+                          it, bad, l_run, m_ref, quarter, lane, rank);
             if (warp == kMergeWarp0) {
                 if (!wait_warp(ctl, bar(ctl, B_EPI), ii & 1)) break;
                 if (lane == 0) mbar_arrive(bar(ctl, B_VEMPTY + p_last));
