@@ -24,14 +24,14 @@ constexpr int kDrow = kDl + kDr;         // 576 values per cached row
 constexpr int kPage = MLA_PAGE_SIZE;     // tokens per cache page
 constexpr uint32_t kPlanMagic = 0x31414c4du;  // "MLA1"
 
-// Planner tuning, in units of one cache page of work (about 1.2 us of an SM
+// Planner tuning, in units of one cache page of work (about 1.1 us of an SM
 // pair on this part): the fixed cost of a work item (query load, pipeline
 // fill, epilogue), the shortest split, and the extra cost of splitting at all
-// (fp32 partials written and merged).  A least-squares fit of every unit's
-// end time against its pages and items gave about five pages per item, but
-// the kernel's end (its slowest unit, with the units sharing the memory
-// system) came out best at ten on the mixed workload.
-constexpr int kItemCost = 10;
+// (fp32 partials written and merged).  Per-unit end times on the mixed
+// workload put an item at about 6 us (5.7 pages) and a page at 1.05 us; of
+// 5, 6, 7, 8 and 10 pages per item, 7 gave the earliest kernel end on the
+// mixed, MTP and long workloads (the slowest unit decides it).
+constexpr int kItemCost = 7;
 constexpr int kMinSplitPages = 8;
 constexpr int kSplitPenalty = 8;
 
