@@ -9,14 +9,17 @@
  *
  *   [0, 512)    e4m3 codes of c_kv[i] / s, i < 512 (round to nearest even,
  *               saturating at +-448)
- *   [512, 640)  k_rope, the 64 bf16 values copied unchanged
+ *   [512, 640)  k_rope[i] / s, i < 64, as bf16 (round to nearest even)
  *   [640, 644)  s = max_i |c_kv[i]| / 448 as fp32 (1 for an all-zero c_kv)
  *   [644, 656)  zero
  *
- * s and every quotient c_kv[i] / s are correctly rounded fp32 values, so the
- * codes are a function of the bf16 row alone.  A row's c_kv is recovered as
- * value(code) * s, within half an e4m3 step (2^-4 of the row's largest
- * magnitude).  Rows must be finite.
+ * s and every quotient (c_kv[i] / s, k_rope[i] / s) are correctly rounded
+ * fp32 values, so the row is a function of the bf16 row alone.  The whole
+ * 576-value row dequantises by the one factor s: c_kv as value(code) * s,
+ * within half an e4m3 step (2^-4 of the row's largest magnitude), k_rope as
+ * value(bf16) * s, within half a bf16 step.  One factor for the whole row
+ * lets a kernel form a score with one contraction over all 576 values and
+ * scale it once.  Rows must be finite.
  *
  * Conventions (as in mla_decode.h): device pointers, caller-owned buffers,
  * work enqueued on `stream`, nothing synchronises; host argument errors

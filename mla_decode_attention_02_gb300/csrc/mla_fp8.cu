@@ -4,7 +4,8 @@
 // 16-byte loads; the row's max |c_kv| is a warp max (exact), s = max / 448 and
 // each quotient c_kv / s are IEEE fp32 divisions, and the hardware conversion
 // rounds each quotient to the nearest e4m3 code (ties to even, saturating).
-// Lanes 0-7 copy k_rope, lane 8 writes s and the zero padding.  Memory-bound:
+// Lanes 0-7 write k_rope / s (fp32 division, rounded to bf16), lane 8 writes s
+// and the zero padding.  Memory-bound:
 // 1152 bytes read and 656 written per row, all 16-byte accesses.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -60,7 +61,16 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) mla_quantize_fp8_kernel(cons
     }
     reinterpret_cast<uint4 *>(dst)[lane] = make_uint4(c[0], c[1], c[2], c[3]);
     if (lane < kDr * 2 / 16) {
-        reinterpret_cast<uint4 *>(dst + kDl)[lane] = reinterpret_cast<const uint4 *>(src + kDl * 2)[lane];
+        const uint4 r = reinterpret_cast<const uint4 *>(src + kDl * 2)[lane];
+        uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rw[j]));
+            const __nv_bfloat162 h = __halves2bfloat162(__float2bfloat16_rn(__fdiv_rn(f.x, s)),
+                                                        __float2bfloat16_rn(__fdiv_rn(f.y, s)));
+            rw[j] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(dst + kDl)[lane] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
     } else if (lane == kDr * 2 / 16) {
         reinterpret_cast<uint4 *>(dst + kDl + kDr * 2)[0] = make_uint4(__float_as_uint(s), 0u, 0u, 0u);
     }

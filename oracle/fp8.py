@@ -8,11 +8,12 @@ section 8: KV-cache-only quantisation of the attention and MLAProlog
 operators), in the form this hardware has native arithmetic for: each cached
 row's 512 c_kv values stored as e4m3 codes of c_kv / s with one fp32 scale per
 token, s = max |c_kv| / 448 (448 is e4m3's largest finite value; s = 1 for an
-all-zero row), and the 64 k_rope values kept in bf16.
+all-zero row), and the 64 k_rope values divided by the same s and kept in
+bf16, so that the whole row dequantises by one factor.
 
 Row layout (656 bytes, a multiple of 16): bytes [0, 512) the codes,
-[512, 640) k_rope (bf16, the bf16 cache's bytes), [640, 644) s (fp32,
-little-endian), [644, 656) zero.
+[512, 640) k_rope / s (bf16: the correctly rounded fp32 quotient rounded to
+nearest even), [640, 644) s (fp32, little-endian), [644, 656) zero.
 
 The codes are decided in fp32, the precision the GPU decides them in: s is the
 correctly rounded fp32 quotient of fp32(max |c_kv|) by 448, each value's
@@ -86,21 +87,23 @@ def quantize_cache(kv_bf16) -> np.ndarray:
     R = codes.shape[0]
     out = np.zeros((R, ROW_BYTES), dtype=np.uint8)
     out[:, :512] = codes
-    rope = kv_bf16.detach().cpu().reshape(R, -1)[:, 512:].contiguous().view(torch.int16).numpy()
-    out[:, 512:640] = rope.view(np.uint8).reshape(R, 128)
+    rope = kv_bf16.detach().cpu().reshape(R, -1)[:, 512:].to(torch.float32).numpy()
+    rope_s = (rope / s[:, None]).astype(np.float32)           # correctly rounded fp32 quotients
+    rope_b = torch.from_numpy(rope_s).to(torch.bfloat16)      # round to nearest even
+    out[:, 512:640] = rope_b.contiguous().view(torch.int16).numpy().view(np.uint8).reshape(R, 128)
     out[:, 640:644] = s.astype("<f4").view(np.uint8).reshape(R, 4)
     return out.reshape(lead + (ROW_BYTES,))
 
 
 def dequantize_cache(fp8_cache) -> np.ndarray:
-    """fp64 [..][576] rows of an fp8 cache: codes x scale, then k_rope."""
+    """fp64 [..][576] rows of an fp8 cache: (codes, then the bf16 k_rope / s) x scale."""
     c = np.asarray(fp8_cache, dtype=np.uint8)
     lead = c.shape[:-1]
     c = c.reshape(-1, ROW_BYTES)
     s = c[:, 640:644].copy().view("<f4").reshape(-1).astype(np.float64)
     lat = e4m3_value(c[:, :512]) * s[:, None]
     rope_bits = c[:, 512:640].copy().view("<u2").astype(np.uint32) << 16
-    rope = rope_bits.view(np.float32).astype(np.float64)
+    rope = rope_bits.view(np.float32).astype(np.float64) * s[:, None]
     return np.concatenate([lat, rope], axis=1).reshape(lead + (576,))
 
 

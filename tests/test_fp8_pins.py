@@ -57,13 +57,21 @@ def test_quantize_cache_layout_and_scale():
     amax = np.abs(lat).max(1)
     np.testing.assert_array_equal(s[amax > 0], (amax[amax > 0] / np.float32(448)).astype(np.float32))
     assert s[1 * 64 + 5] == 1.0 and np.all(rows[1 * 64 + 5, :512] == 0)
-    # the largest value of each row lands on the largest code, k_rope bytes are copied
+    # the largest value of each row lands on the largest code; k_rope is stored divided by s
+    # (correctly rounded fp32 quotient, then bf16 round to nearest even: checked bit by bit
+    # against an integer rounding of the fp32 bits)
     top = np.abs(lat).argmax(1)
     assert np.all(rows[np.arange(rows.shape[0]), top][amax > 0] & 0x7F == 0x7E)
-    np.testing.assert_array_equal(rows[:, 512:640].copy().view("<u2"),
-                                  kv.reshape(-1, 576)[:, 512:].contiguous().view(torch.int16).numpy().view(np.uint16))
+    rope = kv.reshape(-1, 576)[:, 512:].float().numpy()
+    qbits = (rope / s[:, None]).astype(np.float32).view(np.uint32).astype(np.uint64)
+    rne = ((qbits + 0x7FFF + ((qbits >> 16) & 1)) >> 16).astype(np.uint16)
+    np.testing.assert_array_equal(rows[:, 512:640].copy().view("<u2"), rne)
     deq = F.dequantize_cache(q)
-    np.testing.assert_array_equal(deq[..., 512:], kv[..., 512:].double().numpy())
+    ropeq = (rne.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(deq.reshape(-1, 576)[:, 512:], ropeq * s[:, None].astype(np.float64))
+    assert np.all(deq.reshape(-1, 576)[1 * 64 + 5, 512:] == rope[1 * 64 + 5])   # s = 1: k_rope unchanged
+    rrel = np.abs(deq.reshape(-1, 576)[:, 512:] - rope) / np.maximum(np.abs(rope), 1e-30)
+    assert rrel[rope != 0].max() <= 2.0 ** -8 * (1 + 1e-6)  # bf16 rounding of the quotient and fp32 division
     ref = kv[..., :512].double().numpy()
     err = np.abs(deq[..., :512] - ref)
     assert np.all(err[1, 5] == 0)

@@ -1,5 +1,6 @@
 """The fp8 cache quantiser on cuda:0 vs the oracle: every byte identical (codes are integers decided
-in fp32 on both sides; the scale is a correctly rounded fp32 quotient; k_rope bytes are copied)."""
+in fp32 on both sides; the scale and k_rope / s are correctly rounded fp32 quotients, the latter then
+rounded to bf16 to nearest even on both sides)."""
 
 import numpy as np
 import pytest
