@@ -324,12 +324,13 @@ def _config(w):
                   f"cache {W.cache_bytes(w.seq_lens) / 1e6:.0f} MB"}
 
 
-PER_WORKLOADS = ("mixed", "mtp", "long", "long1m", "uniform+pow2", "mixed+pow2")
+PER_WORKLOADS = ("mixed", "mtp", "long", "long1m", "uniform+pow2", "mixed+pow2", "uniform+fp8",
+                 "mixed+fp8")
 STEP_KERNELS = 3          # launches per step: planner, main kernel, merge
 
 
 def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool, warmup: int,
-             sampler_gpu=None, cpu=None, pow2_max: bool = False):
+             sampler_gpu=None, cpu=None, pow2_max: bool = False, fp8: bool = False):
     """Time plan + decode of workload `w` on `dev`; returns a dict of times and the inputs.
 
     Two timed regions run the same steps, each step after a 256 MiB L2 flush:
@@ -338,7 +339,9 @@ def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool,
     kernels would serialise); (2) events around each kernel, for the per-kernel
     times behind the roofline figure.  Steps are captured in a CUDA graph of K
     steps that is replayed until at least `min_steps` steps and `min_seconds`
-    of step time have run, so that the clock sampler sees the region.
+    of step time have run, so that the clock sampler sees the region.  With `fp8` the
+    cache is first quantised by the library's quantiser (outside the timed region) and
+    the steps decode over the fp8 cache.
     """
     import torch
     import torch.distributed as dist
@@ -347,6 +350,8 @@ def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool,
     if cpu is None:
         cpu = W.make_inputs(w)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    if fp8:
+        d["kv8"] = mla.quantize_cache_fp8(d.pop("kv_cache"))
     B, S = w.batch, w.s_q
     mp = d["block_table"].shape[1]
     ws = torch.empty(mla.workspace_size(B, S, mp), dtype=torch.uint8, device=dev)
@@ -357,8 +362,12 @@ def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool,
 
     def step(events=None):
         p = mla.plan(d["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
-        mla.decode(p, d["q_latent"], d["q_rope"], d["kv_cache"], d["block_table"],
-                   scale=d["scale"], out=out, lse=lse, events=events, pow2_max=pow2_max)
+        if fp8:
+            mla.decode_fp8(p, d["q_latent"], d["q_rope"], d["kv8"], d["block_table"],
+                           scale=d["scale"], out=out, lse=lse, events=events, pow2_max=pow2_max)
+        else:
+            mla.decode(p, d["q_latent"], d["q_rope"], d["kv_cache"], d["block_table"],
+                       scale=d["scale"], out=out, lse=lse, events=events, pow2_max=pow2_max)
         return p
 
     for _ in range(max(3, warmup)):
@@ -452,8 +461,8 @@ def _measure(w, dev, world, min_steps: int, min_seconds: float, use_graph: bool,
             "region_s": t_end - t_start}
 
 
-def _roofline(w, main_ms, peaks, peak_src, traffic):
-    cache_b = W.cache_bytes(w.seq_lens)
+def _roofline(w, main_ms, peaks, peak_src, traffic, fp8: bool = False):
+    cache_b = W.cache_bytes_fp8(w.seq_lens) if fp8 else W.cache_bytes(w.seq_lens)
     fl = W.flops(w.seq_lens, w.s_q)
     hbm_peak = peaks["hbm_gbs"]
     main_gbs = cache_b / (main_ms * 1e-3) / 1e9
@@ -559,15 +568,17 @@ def run_native(args, rank, world, local):
     per_workload = {}
     if not args.no_per_workload:
         for name in PER_WORKLOADS:
-            # "<workload>+pow2": the same workload with power-of-two running maxima
+            # "<workload>+pow2": the same workload with power-of-two running maxima;
+            # "<workload>+fp8": the same workload over the fp8 cache
             base, _, mode = name.partition("+")
             if name == w.name:
                 continue
             wk = W.workload(base)
             r = _measure(wk, dev, world, 20, 0.3, not args.no_graph, 3, sampler_gpu=False,
-                         pow2_max=mode == "pow2")
-            rf = _roofline(wk, r["main_ms"], peaks, peak_src, _ncu_traffic(base) if not mode else None)
-            kb = W.cache_bytes(wk.seq_lens)
+                         pow2_max=mode == "pow2", fp8=mode == "fp8")
+            rf = _roofline(wk, r["main_ms"], peaks, peak_src, _ncu_traffic(base) if not mode else None,
+                           fp8=mode == "fp8")
+            kb = W.cache_bytes_fp8(wk.seq_lens) if mode == "fp8" else W.cache_bytes(wk.seq_lens)
             per_workload[name] = {
                 "config": _config(wk), "steps": r["steps"], "us_per_step": r["step_ms"] * 1e3,
                 "tb_s_step": whole_job_tbs(world, kb, r["step_ms"]),

@@ -44,6 +44,28 @@ extern "C" {
 mla_status mla_cache_quantize_fp8(const void *kv_cache, int64_t num_rows, void *kv_cache_fp8,
                                   mla_stream_t stream);
 
+/*
+ * mla_decode over a paged fp8 cache (kv_cache_fp8: [num_pages][64][656] bytes in
+ * the row format above): the attention of mla_decode on the dequantised rows.
+ * Same problem, schedule (mla_decode_plan), workspace, outputs, scale rule,
+ * flags and error contract as mla_decode; num_pages bounds the block table's
+ * entries as there.  q stays bf16; the kernel turns each page's e4m3 codes into
+ * bf16 operands on the SM (exactly: every e4m3 value is a bf16 value), contracts
+ * q with [codes | k_rope / s] in fp32, multiplies each score by its token's s,
+ * and folds s into each attention weight before the weight is rounded to bf16
+ * for the contraction with the codes.  The roundings are thus those of
+ * mla_decode (bf16 weights, fp32 accumulation, bf16 o_latent), moved by the
+ * factor s, and the result is the dequantised cache's attention to that
+ * accuracy.  Half the cache bytes per token (656 against 1152).  The cache
+ * pointer must be 16-byte aligned.  events: NULL, or 3 cudaEvent_t handles
+ * recorded as mla_decode_timed records them (before the main kernel, before
+ * the merge, after the merge; NULL entries skipped).
+ */
+mla_status mla_decode_fp8(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                          const void *kv_cache_fp8, int64_t num_pages, const int32_t *block_table,
+                          float scale, void *o_latent, float *lse, void *workspace,
+                          size_t workspace_bytes, mla_stream_t stream, void *const *events);
+
 #ifdef __cplusplus
 }
 #endif

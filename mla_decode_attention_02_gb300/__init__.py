@@ -23,7 +23,7 @@ and the step after it (``include/mla_epilog.h``) projects the heads back out:
 from ._binding import (D_V, HIDDEN, DEFAULT_ROPE_BASE, DEFAULT_RMS_EPS, DEFAULT_SCALE, D_LATENT, D_NOPE, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
                        MLA_DEV_BAD_PAGE, MLA_DEV_BAD_PLAN, MLA_DEV_BAD_SEQ_LEN, MLA_DEV_TIMEOUT,
                        MLAError, MLA_FLAG_POW2_MAX, MLA_INJECT_WITHHOLD_K_LOAD, NOALLOC_SCRATCH_BYTES, Plan, check, decode,
-                       decode_diag, decode_noalloc, epilog_oproj, epilog_uv, quantize_cache_fp8,
+                       decode_diag, decode_fp8, decode_noalloc, epilog_oproj, epilog_uv, quantize_cache_fp8,
                        load_library, num_units, parse_plan, plan, prolog, rope_table,
                        plan_device_bytes, plan_host, plan_layout, workspace_size)
 
@@ -32,6 +32,6 @@ __all__ = ["D_V", "HIDDEN", "epilog_oproj", "epilog_uv",
            "DEFAULT_ROPE_BASE", "DEFAULT_RMS_EPS", "DEFAULT_SCALE", "D_LATENT", "D_NOPE", "D_ROPE", "LIB_PATH", "NUM_HEADS", "PAGE_SIZE",
            "MLA_DEV_BAD_PAGE", "MLA_DEV_BAD_PLAN", "MLA_DEV_BAD_SEQ_LEN", "MLA_DEV_TIMEOUT",
            "MLAError", "MLA_FLAG_POW2_MAX", "MLA_INJECT_WITHHOLD_K_LOAD", "NOALLOC_SCRATCH_BYTES", "Plan", "check", "decode",
-           "decode_diag", "decode_noalloc",
+           "decode_diag", "decode_fp8", "decode_noalloc",
            "load_library", "num_units", "parse_plan",
            "plan", "plan_device_bytes", "prolog", "rope_table", "plan_host", "plan_layout", "workspace_size"]

@@ -59,6 +59,8 @@ _SIGS = {
     "mla_decode_diag": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_float,
                                        _vp, _vp, _vp, ctypes.c_size_t, _vp, ctypes.c_uint64,
                                        ctypes.c_uint32]),
+    "mla_decode_fp8": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_float, _vp,
+                                      _vp, _vp, ctypes.c_size_t, _vp, _vp]),
     "mla_decode_noalloc": (ctypes.c_int, [_P, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
                                           ctypes.c_float, _vp, _vp, _vp]),
     "mla_decode_check": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
@@ -194,6 +196,16 @@ def decode(p: Plan, q_latent, q_rope, kv_cache, block_table, *, scale: float = D
                    MLA_FLAG_POW2_MAX if pow2_max else 0)
 
 
+def decode_fp8(p: Plan, q_latent, q_rope, kv_cache_fp8, block_table, *, scale: float = DEFAULT_SCALE,
+               out=None, lse=None, stream=None, events=None, pow2_max: bool = False):
+    """``mla_decode_fp8``: decode over an fp8 cache (uint8 [num_pages][64][656]) -> (o bf16, lse fp32).
+
+    events and pow2_max as in ``decode``.
+    """
+    return _decode(p, q_latent, q_rope, kv_cache_fp8, block_table, scale, out, lse, stream, events, None,
+                   MLA_FLAG_POW2_MAX if pow2_max else 0, fp8=True)
+
+
 MLA_INJECT_WITHHOLD_K_LOAD = 0x1
 
 
@@ -209,15 +221,21 @@ def decode_diag(p: Plan, q_latent, q_rope, kv_cache, block_table, *, wait_limit_
                    (int(wait_limit_ns), int(inject)), 0)
 
 
-def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, diag, flags):
+def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream, events, diag, flags,
+            fp8=False):
     import torch
     dev = p.workspace.device
     B, S = p.batch, p.s_q
     _req(q_latent, "q_latent", torch.bfloat16, (B, S, NUM_HEADS, D_LATENT), dev)
     _req(q_rope, "q_rope", torch.bfloat16, (B, S, NUM_HEADS, D_ROPE), dev)
-    _req(kv_cache, "kv_cache", torch.bfloat16, None, dev)
-    if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE_SIZE, D_LATENT + D_ROPE):
-        raise ValueError("kv_cache must be [num_pages][64][576]")
+    if fp8:
+        _req(kv_cache, "kv_cache_fp8", torch.uint8, None, dev)
+        if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE_SIZE, FP8_ROW_BYTES):
+            raise ValueError("kv_cache_fp8 must be [num_pages][64][656] bytes")
+    else:
+        _req(kv_cache, "kv_cache", torch.bfloat16, None, dev)
+        if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE_SIZE, D_LATENT + D_ROPE):
+            raise ValueError("kv_cache must be [num_pages][64][576]")
     _req(block_table, "block_table", torch.int32, (B, p.max_pages), dev)
     if out is None:
         out = torch.empty((B, S, NUM_HEADS, D_LATENT), dtype=torch.bfloat16, device=dev)
@@ -229,16 +247,20 @@ def _decode(p, q_latent, q_rope, kv_cache, block_table, scale, out, lse, stream,
     args = [ctypes.byref(prob), q_latent.data_ptr(), q_rope.data_ptr(), kv_cache.data_ptr(),
             kv_cache.shape[0], block_table.data_ptr(), float(scale), out.data_ptr(),
             lse.data_ptr(), p.workspace.data_ptr(), p.workspace.numel(), _stream_handle(stream)]
+    handles = None
+    if events is not None:
+        if len(events) != 3:
+            raise ValueError("events must hold three torch.cuda.Event")
+        handles = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) if e is not None
+                                          else None for e in events])
     with torch.cuda.device(dev):
-        if diag is not None:
+        if fp8:
+            _check(load_library().mla_decode_fp8(*args, handles), "mla_decode_fp8")
+        elif diag is not None:
             _check(load_library().mla_decode_diag(*args, *diag), "mla_decode_diag")
-        elif events is None:
+        elif handles is None:
             _check(load_library().mla_decode(*args), "mla_decode")
         else:
-            if len(events) != 3:
-                raise ValueError("events must hold three torch.cuda.Event")
-            handles = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) if e is not None
-                                              else None for e in events])
             _check(load_library().mla_decode_timed(*args, handles), "mla_decode_timed")
     return out, lse
 
@@ -432,7 +454,7 @@ def quantize_cache_fp8(kv_cache, *, out=None, stream=None):
     """The fp8 (e4m3) cache of a bf16 cache (``mla_cache_quantize_fp8``).
 
     kv_cache [..][576] bf16 -> uint8 [..][656]: per row the 512 e4m3 codes of c_kv / s,
-    k_rope (bf16 bytes), s (fp32), zero padding.
+    k_rope / s (bf16), s (fp32), zero padding.
     """
     import torch
     if kv_cache.shape[-1] != D_LATENT + D_ROPE:

@@ -23,7 +23,7 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
                         int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags,
-                        uint32_t flags, cudaStream_t stream);
+                        uint32_t flags, bool fp8, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // a bounded device wait gives up after 2 s
 }  // namespace mla
 
@@ -146,7 +146,7 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
                               float scale, void *o_latent, float *lse, void *workspace,
                               size_t workspace_bytes, mla_stream_t stream, void *const *events,
                               uint64_t wait_limit_ns = mla::kDefaultWaitLimitNs,
-                              uint32_t test_flags = 0) {
+                              uint32_t test_flags = 0, bool fp8 = false) {
     mla_status st = mla::check_decode_args(prob, q_latent, q_rope, kv_cache, num_pages, block_table,
                                            nullptr, false, scale, o_latent, lse, workspace,
                                            workspace_bytes, true);
@@ -171,7 +171,7 @@ static mla_status decode_impl(const mla_problem *prob, const void *q_latent, con
     cudaError_t e = mla::launch_main(q_latent, q_rope, kv_cache, num_pages, block_table, scale,
                                      workspace, o_latent, lse, prob->batch, prob->s_q,
                                      prob->max_pages_per_seq, units, wait_limit_ns, test_flags,
-                                     (uint32_t)prob->flags, s);
+                                     (uint32_t)prob->flags, fp8, s);
     if (e != cudaSuccess || !mark(1)) return MLA_ERR_CUDA;
     e = mla::launch_combine(workspace, o_latent, lse, prob->batch, prob->s_q, units, s);
     if (e != cudaSuccess || !mark(2)) return MLA_ERR_CUDA;
@@ -203,6 +203,14 @@ mla_status mla_decode_diag(const mla_problem *prob, const void *q_latent, const 
     if (inject & ~MLA_INJECT_WITHHOLD_K_LOAD) return MLA_ERR_INVALID_ARG;
     return decode_impl(prob, q_latent, q_rope, kv_cache, num_pages, block_table, scale, o_latent,
                        lse, workspace, workspace_bytes, stream, nullptr, wait_limit_ns, inject);
+}
+
+mla_status mla_decode_fp8(const mla_problem *prob, const void *q_latent, const void *q_rope,
+                          const void *kv_cache_fp8, int64_t num_pages, const int32_t *block_table,
+                          float scale, void *o_latent, float *lse, void *workspace,
+                          size_t workspace_bytes, mla_stream_t stream, void *const *events) {
+    return decode_impl(prob, q_latent, q_rope, kv_cache_fp8, num_pages, block_table, scale, o_latent,
+                       lse, workspace, workspace_bytes, stream, events, mla::kDefaultWaitLimitNs, 0, true);
 }
 
 mla_status mla_decode_check(const void *workspace, int32_t *device_status, mla_stream_t stream) {

@@ -57,13 +57,30 @@
 // right after the softmax's TMEM load, so the next page's score MMAs wait
 // only for that.  Every wait is bounded: on time-out the kernel records
 // MLA_DEV_TIMEOUT and winds down instead of hanging.
+//
+// fp8 cache (the same kernel, kFp8 = true, 512 threads): the K load brings the
+// 32 tokens' e4m3 codes (16 KB) into the upper half of the stage's latent
+// blocks, k_rope / s (bf16) into its place, and the tokens' scales into a
+// four-slot ring; the V load brings the codes of the CTA's 256 dims (16 KB)
+// into the upper half of the V stage.  Warps 12-13 expand each K stage and
+// warps 14-15 each V stage in place into the bf16 layout above (exact: every
+// e4m3 value is a bf16 value), then release it to the MMAs.  The softmax
+// multiplies each score by its token's s and folds s into the token's weight
+// before rounding it to bf16, so both contractions see the codes themselves.
+// The expansion lengthens each stage's load-to-MMA chain on the two-stage
+// rings, which sets this variant's page rate (about twice the bf16 cache's
+// time per page, measured): the fp8 cache halves the bytes held per token,
+// not the time.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
+#include "mla_fp8.h"
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -106,6 +123,17 @@ constexpr uint32_t kOffP = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffRef = kOffP + kPSlots * kPSlotBytes;   // agreed max, kRefLag x 128 floats
 constexpr uint32_t kOffBar = kOffRef + kRefLag * 512;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers, + alignment slack
+// fp8 cache (variant of the same kernel): four more warps convert each landed K
+// and V stage from e4m3 codes to the bf16 layout above, and each K load brings
+// this CTA's 32 tokens' scales (16 bytes per token) into a ring after the barriers
+constexpr int kThreadsFp8 = 512;
+constexpr int kConvWarp0 = 12;                      // warps 12-15 (fp8 only)
+constexpr uint32_t kScaleStage = kHalfTok * 16;     // 512 bytes per page
+constexpr int kScaleSlots = 4;                      // page mod 4, freed by the softmax
+constexpr uint32_t kOffScale = kOffBar + 512;
+constexpr uint32_t kSmemBytesFp8 = kOffScale + kScaleSlots * kScaleStage + 1024;
+static_assert(kSmemBytesFp8 <= 232448, "shared memory budget (fp8)");
+static_assert(kOffScale % 128 == 0, "scale ring alignment");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 &&
                   kKStageBytes % 1024 == 0 && kVStageBytes % 1024 == 0 && kPSlotBytes % 1024 == 0,
               "TMA/UMMA tile alignment");
@@ -145,7 +173,10 @@ enum : uint32_t {
     B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx)
     B_QCOPIED = B_QSTAGE + 1,            // item start: softmax warps moved the staged q to TMEM
     B_QTILE = B_QCOPIED + 1,             // q dims 384-575 landed in the shared-memory q tile (+tx)
-    B_COUNT = B_QTILE + 1,
+    B_KCONV = B_QTILE + 1,               // fp8: + page parity: K stage converted to bf16
+    B_VCONV = B_KCONV + 2,               // fp8: + page parity: V stage converted to bf16
+    B_SCEMPTY = B_VCONV + 2,             // fp8: + page mod 4: the softmax is done with the scales
+    B_COUNT = B_SCEMPTY + kScaleSlots,
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 
@@ -157,6 +188,10 @@ struct Params {
     // [block][token][64 dims], the layout the MMAs read
     CUtensorMap tm_k;       // box 64 x 32 x 9 x 1: a token half, all 576 dims
     CUtensorMap tm_v;       // box 64 x 64 x 4 x 1: all 64 tokens, one CTA's 256 output dims
+    // fp8 cache: tm_k / tm_v are views of the e4m3 codes (128 codes, 64 tokens, 4 blocks,
+    // pages; box 128 x 32 x 4 x 1 and 128 x 64 x 2 x 1), and
+    CUtensorMap tm_kr;      // k_rope / s: (64 values, 64 tokens, pages), box 64 x 32 x 1, bf16
+    CUtensorMap tm_ks;      // s: (4 floats, 64 tokens, pages), box 4 x 32 x 1
     const __nv_bfloat16 *q_latent;
     const int32_t *block_table;
     uint8_t *ws;
@@ -428,7 +463,58 @@ __device__ __noinline__ void item_epilogue(const Ctl ctl, __nv_bfloat16 *o_laten
     if (lane == 0) mbar_arrive(bar(ctl, B_EPI));
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// One converter thread's share of a stage (64 threads per stage): the stage's
+// first 16 KB of latent space receives 16 KB of e4m3 codes in its upper half as
+// [16 KB / (kRows * 128) code blocks of 128 codes][kRows tokens][128 bytes], and
+// becomes [2 x that many bf16 blocks of 64 dims][kRows tokens][128 bytes]; both
+// are 128-byte swizzled (16-byte chunk c of a row at c ^ (row & 7)).  Thread t
+// reads code rows t and t + 64 into registers, meets the other converter warp
+// at named barrier `bar_id`, then writes its four bf16 rows.
+template <int kRows>
+__device__ __forceinline__ void convert_codes(uint8_t *stage, int t, int bar_id) {
+    static_assert((16384 / (kRows * 128)) * kRows == 128, "128 code rows per stage");
+    const uint8_t *codes = stage + 16384;
+    uint4 x[2][8];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int R = t + 64 * rr;            // code row: block R / kRows, token R % kRows
+        const int tok = R % kRows;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            x[rr][c] = *reinterpret_cast<const uint4 *>(codes + R * 128 + ((c ^ (tok & 7)) << 4));
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int R = t + 64 * rr;
+        const int b8 = R / kRows, tok = R % kRows;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            // 16 codes = dims 16c .. 16c + 15 of code block b8 -> bf16 block 2 b8 + c / 4,
+            // chunks 2 (c % 4) and 2 (c % 4) + 1 of its row
+            const uint32_t w[4] = {x[rr][c].x, x[rr][c].y, x[rr][c].z, x[rr][c].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                // e4m3 -> f16 -> f32 -> bf16: each step exact (an e4m3 value has at
+                // most 4 significant bits and lies within both formats' normal range)
+                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xFFFFu), __NV_E4M3);
+                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
+                const float2 flo = __half22float2(__half2(lo));
+                const float2 fhi = __half22float2(__half2(hi));
+                o[2 * q] = pack_bf16(flo.x, flo.y);
+                o[2 * q + 1] = pack_bf16(fhi.x, fhi.y);
+            }
+            uint8_t *row = stage + (2 * b8 + c / 4) * (kRows * 128) + tok * 128;
+            const int cb = 2 * (c % 4);
+            *reinterpret_cast<uint4 *>(row + ((cb ^ (tok & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + (((cb + 1) ^ (tok & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 mla_main_tc_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -459,6 +545,11 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
         abort_flag = 0;
         mbar_init(bar(ctl, B_Q_FULL), 4);
         mbar_init(bar(ctl, B_QTILE), 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bar(ctl, B_KCONV + p), 2);   // its two converter warps
+            mbar_init(bar(ctl, B_VCONV + p), 2);
+        }
+        for (int q = 0; q < kScaleSlots; ++q) mbar_init(bar(ctl, B_SCEMPTY + q), 4);
         mbar_init(bar(ctl, B_QSTAGE), 1);
         mbar_init(bar(ctl, B_QCOPIED), 4);
         mbar_init(bar(ctl, B_Q_EMPTY), 1);
@@ -578,12 +669,29 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                             ok = false;
                             break;
                         }
+                        if (kFp8 && g >= (uint32_t)kScaleSlots &&
+                            !wait_warp(ctl, bar(ctl, B_SCEMPTY + g % kScaleSlots), ((g / kScaleSlots) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
                         if (lane == 0 && !(withhold && g == 1)) {
                             // one 36 KB box: an SM ingests a few large TMA copies much
                             // faster than many 4 KB ones
                             const uint32_t fa = bar(ctl, B_KFULL + p);
-                            mbar_arrive_expect_tx(fa, kKStageBytes);
-                            tma_load_4d(s_k + p * kKStageBytes, &P.tm_k, 0, tok_own, 0, page, fa);
+                            if constexpr (kFp8) {
+                                // the codes (16 KB) into the upper half of the stage's latent
+                                // blocks, k_rope / s (4 KB) into its place (the converter
+                                // warps expand the codes downward), the tokens' scales into
+                                // the ring (its slot was freed above)
+                                mbar_arrive_expect_tx(fa, 4 * kBox + kBox + kScaleStage);
+                                tma_load_4d(s_k + p * kKStageBytes + 4 * kBox, &P.tm_k, 0, tok_own, 0, page, fa);
+                                tma_load_3d(s_k + p * kKStageBytes + 8 * kBox, &P.tm_kr, 0, tok_own, page, fa);
+                                tma_load_3d(s_base + kOffScale + (g % kScaleSlots) * kScaleStage, &P.tm_ks, 0,
+                                            tok_own, page, fa);
+                            } else {
+                                mbar_arrive_expect_tx(fa, kKStageBytes);
+                                tma_load_4d(s_k + p * kKStageBytes, &P.tm_k, 0, tok_own, 0, page, fa);
+                            }
                         }
                         issued = g + 1;
                         if (k0 + kk == 0) {
@@ -620,8 +728,16 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         }
                         if (lane == 0) {
                             const uint32_t fv = bar(ctl, B_VFULL + p);
-                            mbar_arrive_expect_tx(fv, kVStageBytes);
-                            tma_load_4d(s_v + p * kVStageBytes, &P.tm_v, 0, 0, 4 * (int)rank, page, fv);
+                            if constexpr (kFp8) {
+                                // the codes of this CTA's 256 output dims (16 KB) into the upper
+                                // half of the stage (the scales came with the page's K load)
+                                mbar_arrive_expect_tx(fv, kVStageBytes / 2);
+                                tma_load_4d(s_v + p * kVStageBytes + kVStageBytes / 2, &P.tm_v, 0, 0, 2 * (int)rank,
+                                            page, fv);
+                            } else {
+                                mbar_arrive_expect_tx(fv, kVStageBytes);
+                                tma_load_4d(s_v + p * kVStageBytes, &P.tm_v, 0, 0, 4 * (int)rank, page, fv);
+                            }
                         }
                         issued = g + 1;
                     }
@@ -668,7 +784,8 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     // the softmax has read the scores of page g - 2 from it
                     const uint32_t ko = p * kKStageBytes;
                     const uint32_t tSp = tS + kHalfTok * p;
-                    if (!wait_warp(ctl, bar(ctl, B_KFULL + p), (g >> 1) & 1)) { ok = false; break; }
+                    // (fp8: the stage is read once the converter warps turned its codes into bf16)
+                    if (!wait_warp(ctl, bar(ctl, (kFp8 ? B_KCONV : B_KFULL) + p), (g >> 1) & 1)) { ok = false; break; }
                     if (g >= 2 && !wait_warp(ctl, bar(ctl, B_SEMPTY + p), ((g >> 1) - 1) & 1)) {
                         ok = false;
                         break;
@@ -695,7 +812,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     // warps released the P slot
                     const uint32_t ps = g % kPSlots, pu = g / kPSlots;
                     const uint32_t vo = p * kVStageBytes, po = ps * kPSlotBytes;
-                    if (!wait_warp(ctl, bar(ctl, B_VFULL + p), (g >> 1) & 1) ||
+                    if (!wait_warp(ctl, bar(ctl, (kFp8 ? B_VCONV : B_VFULL) + p), (g >> 1) & 1) ||
                         !wait_warp(ctl, bar(ctl, B_PREADY + ps), pu & 1)) {
                         ok = false;
                         break;
@@ -824,6 +941,13 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
 
                 const int valid = (k == n - 1) ? valid_last : kPage;
                 const int v_own = min(max(valid - tok_own, 0), kHalfTok);
+                // fp8 cache: the score MMAs contracted q with the codes and k_rope / s, so
+                // each token's raw score is multiplied by its scale s (> 0)
+                const float *tsc = reinterpret_cast<const float *>(smem + kOffScale + (g % kScaleSlots) * kScaleStage);
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * tsc[4 * j]);
+                }
                 // scores in log2 units are r * scale_log2 (scale > 0, so the max of
                 // the raw scores gives the max); masked tokens (ragged last page)
                 // are -inf
@@ -854,7 +978,19 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                     const float e0 = fast_exp2(fmaf(__uint_as_float(r[2 * j]), sc, -mu));
                     const float e1 = fast_exp2(fmaf(__uint_as_float(r[2 * j + 1]), sc, -mu));
                     rsum += e0 + e1;
-                    pk[j] = pack_bf16(e0, e1);
+                    if constexpr (kFp8) {
+                        // PV contracts with the codes: each weight carries its token's
+                        // scale (masked tokens stay 0 whatever their scale slot holds)
+                        pk[j] = pack_bf16(2 * j < v_own ? e0 * tsc[8 * j] : 0.f,
+                                          2 * j + 1 < v_own ? e1 * tsc[8 * j + 4] : 0.f);
+                    } else {
+                        pk[j] = pack_bf16(e0, e1);
+                    }
+                }
+                // the scales of this page are no longer needed
+                if constexpr (kFp8) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(ctl, B_SCEMPTY + g % kScaleSlots));
                 }
                 l_own = l_own * l_scale + rsum;
                 // the P slot is free in both CTAs once PV of page g - kPSlots is done
@@ -883,7 +1019,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                 if (lane == 0) mbar_arrive(bar(ctl, B_SDONE + ps));
             }
         }
-    } else {
+    } else if (warp < kMergeWarp0 + 4) {
         // ------------------------------------------------------------ merge + epilogue warps
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
@@ -1006,6 +1142,31 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             }
             __syncwarp();
         }
+    } else if constexpr (kFp8) {
+        // ------------------------------------------------------------ fp8 -> bf16 converters
+        // Warps 12-13 expand each landed K stage, warps 14-15 each V stage, in place:
+        // the codes sit in the upper half of the stage's latent blocks; every thread
+        // reads its two 128-byte code rows, the pair of warps meets at a named barrier,
+        // then writes the bf16 rows over the whole stage.  e4m3 values are exact in bf16.
+        const bool kside = warp < kConvWarp0 + 2;
+        const int ct = (warp - (kside ? kConvWarp0 : kConvWarp0 + 2)) * 32 + lane;   // 0..63
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = i_begin; i < i_end && ok; ++i) {
+            const int n = (items[i].kv_end - items[i].kv_begin + kPage - 1) / kPage;
+            for (int k = 0; k < n; ++k, ++g) {
+                const uint32_t p = g & 1;
+                if (!wait_warp(ctl, bar(ctl, (kside ? B_KFULL : B_VFULL) + p), (g >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (kside) convert_codes<kHalfTok>(smem + kOffK + p * kKStageBytes, ct, 1);
+                else convert_codes<kPage>(smem + kOffV + p * kVStageBytes, ct, 2);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ctl, (kside ? B_KCONV : B_VCONV) + p));
+            }
+        }
     }
 
     // teardown: both CTAs finish (every remote store landed, no remote arrive in
@@ -1036,18 +1197,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz) {
+            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz,
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
-              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, type, rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct DeviceInfo {
     int units = 0;
     bool attr_set = false;
+    int fp8 = 0;   // the fp8 variant: 0 not checked, 1 runs on the same units, -1 does not
 };
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[64];
@@ -1057,7 +1220,7 @@ cudaError_t prepare(int dev, int *units) {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceInfo &d = g_dev[dev];
     if (!d.attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(mla_main_tc_kernel,
+        cudaError_t e = cudaFuncSetAttribute(mla_main_tc_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -1076,7 +1239,7 @@ cudaError_t prepare(int dev, int *units) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, mla_main_tc_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, mla_main_tc_kernel<false>, &cfg);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
         d.units = n;
@@ -1084,6 +1247,34 @@ cudaError_t prepare(int dev, int *units) {
     }
     *units = d.units;
     return cudaSuccess;
+}
+
+// The fp8 variant runs the same schedule, so it must fit as many units.
+cudaError_t prepare_fp8(int dev, int units) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (d.fp8 == 0) {
+        cudaError_t e = cudaFuncSetAttribute(mla_main_tc_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytesFp8);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kClusterSize * units);
+        cfg.blockDim = dim3(kThreadsFp8);
+        cfg.dynamicSmemBytes = kSmemBytesFp8;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = kClusterSize;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, mla_main_tc_kernel<true>, &cfg);
+        if (e != cudaSuccess) return e;
+        d.fp8 = n >= units ? 1 : -1;
+    }
+    return d.fp8 == 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
 }  // namespace
@@ -1103,7 +1294,14 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
                         int64_t num_pages, const int32_t *block_table, float scale, void *ws,
                         void *o_latent, float *lse, int32_t batch, int32_t s_q, int32_t max_pages,
                         int32_t num_units, uint64_t wait_limit_ns, uint32_t test_flags, uint32_t flags,
-                        cudaStream_t stream) {
+                        bool fp8, cudaStream_t stream) {
+    if (fp8) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = prepare_fp8(dev, num_units);
+        if (e != cudaSuccess) return e;
+    }
     Params p;
     const cuuint64_t qrows = (cuuint64_t)batch * s_q * kHeads;
     {
@@ -1120,7 +1318,30 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
         if (!encode(&p.tm_q_rope, q_rope, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    {
+    if (fp8) {
+        // 656-byte rows: the codes as (128 codes, token, 128-code block, page), the
+        // block stride (128 bytes) below the row stride; k_rope / s (bf16) at byte 512
+        // and the scale (fp32) at byte 640 of each row
+        const uint8_t *kv8 = static_cast<const uint8_t *>(kv);
+        const cuuint64_t row = MLA_FP8_ROW_BYTES, pg = row * kPage;
+        cuuint64_t dims[4] = {128, (cuuint64_t)kPage, 4, (cuuint64_t)num_pages};
+        cuuint64_t strides[3] = {row, 128, pg};
+        cuuint32_t box_k[4] = {128, (cuuint32_t)kHalfTok, 4, 1};
+        cuuint32_t box_v[4] = {128, (cuuint32_t)kPage, 2, 1};
+        cuuint64_t rdims[3] = {64, (cuuint64_t)kPage, (cuuint64_t)num_pages};
+        cuuint64_t rstrides[2] = {row, pg};
+        cuuint32_t rbox[3] = {64, (cuuint32_t)kHalfTok, 1};
+        cuuint64_t sdims[3] = {4, (cuuint64_t)kPage, (cuuint64_t)num_pages};
+        cuuint32_t sbox[3] = {4, (cuuint32_t)kHalfTok, 1};
+        if (!encode(&p.tm_k, kv8, 4, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+            !encode(&p.tm_v, kv8, 4, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+            !encode(&p.tm_kr, kv8 + kDl, 3, rdims, rstrides, rbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&p.tm_ks, kv8 + kDl + 2 * kDr, 3, sdims, rstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+    } else {
         // (dim within block, token, dim block, page); the block stride (128 bytes) is
         // below the token stride, so a box lands block-major in shared memory
         cuuint64_t dims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)(kDrow / 64), (cuuint64_t)num_pages};
@@ -1148,8 +1369,8 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterSize * num_units);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(fp8 ? kThreadsFp8 : kThreads);
+    cfg.dynamicSmemBytes = fp8 ? kSmemBytesFp8 : kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1160,7 +1381,8 @@ cudaError_t launch_main(const void *q_latent, const void *q_rope, const void *kv
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, mla_main_tc_kernel, p);
+    return fp8 ? cudaLaunchKernelEx(&cfg, mla_main_tc_kernel<true>, p)
+               : cudaLaunchKernelEx(&cfg, mla_main_tc_kernel<false>, p);
 }
 
 }  // namespace mla

@@ -119,8 +119,8 @@ def test_prolog_and_epilog_reject_bad_arguments_before_any_cuda_call():
 
 
 def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
-    """mla_decode_plan, mla_decode, mla_decode_timed, mla_decode_diag and mla_decode_noalloc
-    refuse null or unaligned pointers, an empty page pool, a non-positive or non-finite scale
+    """mla_decode_plan, mla_decode, mla_decode_timed, mla_decode_diag, mla_decode_fp8 and
+    mla_decode_noalloc refuse null or unaligned pointers, an empty page pool, a non-positive or non-finite scale
     and a workspace below the size any device could need (mla_decode_diag also a wait limit
     outside [1 us, 60 s] and unknown injection bits), before they make a CUDA call (so these
     run without a GPU; a call that passed validation would stop at the first CUDA call
@@ -140,6 +140,8 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
                 nbytes, None]
         if timed == "diag":
             return lib.mla_decode_diag(*args, limit, inject)
+        if timed == "fp8":
+            return lib.mla_decode_fp8(*args, None)
         return lib.mla_decode_timed(*args, None) if timed == "timed" else lib.mla_decode(*args)
 
     def noalloc(prob=good, ptrs=(A, A, A), num_pages=8, bt=A, seq=A, scale=0.072, out=(A, A)):
@@ -155,7 +157,7 @@ def test_decode_entry_points_reject_bad_arguments_before_any_cuda_call():
     assert plan(ws=None) == 1
     assert plan(ws=A + 8) == 1
     assert plan(nbytes=64) == 3
-    for timed in ("plain", "timed", "diag"):
+    for timed in ("plain", "timed", "diag", "fp8"):
         assert decode(prob=None, timed=timed) == 1
         assert decode(prob=_prob(heads=64), timed=timed) == 2
         assert decode(ptrs=(None, A, A), timed=timed) == 1

@@ -156,6 +156,14 @@ def cache_bytes(seq_lens) -> int:
     return sum(int(L) for L in seq_lens) * D_ROW * 2
 
 
+FP8_ROW_BYTES = 656   # an fp8 cache row: 512 e4m3 codes, 64 bf16 k_rope / s, fp32 s, padding
+
+
+def cache_bytes_fp8(seq_lens) -> int:
+    """Algorithmic bytes of the same step over the fp8 cache: every 656-byte row once."""
+    return sum(int(L) for L in seq_lens) * FP8_ROW_BYTES
+
+
 def flops(seq_lens, s_q: int) -> int:
     """Tensor FLOPs of one step: 2 * heads * (576 + 512) per (query token, visible key)."""
     per_key = 2 * NUM_HEADS * (D_ROW + D_LATENT)
