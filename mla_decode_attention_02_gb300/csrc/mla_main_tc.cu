@@ -343,17 +343,21 @@ __device__ __noinline__ void scale_p_row(uint8_t *tile, int h, float f) {
     }
 }
 
-// At an item's start q dims 0-255 (four 64-dim blocks, 128 heads each, 128-byte
+// At an item's start q dims 0-319 (five 64-dim blocks, 128 heads each, 128-byte
 // swizzle) come in by TMA through buffers that are free then: blocks 0-1 in the
 // K stage that the item's second page will use (its first page loads into the
-// other one meanwhile), 2-3 in the shared-memory q tile (free once this CTA's
-// score MMAs of the previous item are done).  Loading q through registers costs one L1 wavefront per head
-// row per instruction, so only dims 256-383 take that path, overlapped.
-constexpr int kQStaged = 4;
+// other one meanwhile), 2-4 in the shared-memory q tile (free once this CTA's
+// score MMAs of the previous item are done).  Loading q through registers costs
+// one L1 wavefront per head row per instruction, and those loads delay the
+// shared-memory reads of the copy into TMEM queued behind them (measured: the
+// copy of four staged blocks took 2.1 us behind two register chunks, 0.4 us
+// without), so only dims 320-383 take that path, overlapped.
+constexpr int kQStaged = 5;
 __device__ __forceinline__ uint32_t q_stage_off(int b, uint32_t kstage) {
     return b < 2 ? kOffK + kstage * kKStageBytes + b * kQBlk : kOffQS + (b - 2) * kQBlk;
 }
-static_assert(2 * kQBlk <= kKStageBytes && 2 * kQBlk <= kQSBytes && kQStaged * 64 < kQTDims, "q staging");
+static_assert(2 * kQBlk <= kKStageBytes && (kQStaged - 2) * kQBlk <= kQSBytes && kQStaged * 64 < kQTDims,
+              "q staging");
 
 // Head h's row of staged q block b -> TMEM columns [32 b, 32 b + 32): chunk c
 // (8 dims) of row h sits at c ^ (h & 7); eight consecutive heads read eight

@@ -11,15 +11,14 @@ import workloads as W
 
 m = pytest.importorskip("mla_decode_attention_02_gb300")
 
-MIN_SPLIT = 8
-
-
 def _check_schedule(seq_lens, s_q, units, max_pages=None):
     seq_lens = [int(x) for x in seq_lens]
     if max_pages is None:
         max_pages = max((L + 63) // 64 for L in seq_lens)
     r = m.plan_host(seq_lens, s_q=s_q, max_pages_per_seq=max_pages, num_units=units)
     h, items, ub = r["header"], r["items"], r["unit_begin"]
+    min_split = int(h["min_split"])          # the planner's shortest piece (a tuning constant)
+    assert min_split >= 1
     R = len(seq_lens) * s_q
     assert h["num_rows"] == R and h["num_units"] == units and h["num_items"] == len(items)
     assert h["num_items"] <= h["max_items"]
@@ -40,7 +39,7 @@ def _check_schedule(seq_lens, s_q, units, max_pages=None):
         for j0, j1, part in pieces:
             assert j0 % 64 == 0 and j1 > j0
             if len(pieces) > 1:
-                assert (j1 - j0 + 63) // 64 >= MIN_SPLIT
+                assert (j1 - j0 + 63) // 64 >= min_split
         if len(pieces) == 1:
             assert pieces[0][2] == -1 and r["row_part0"][row] == -1
         else:
@@ -66,7 +65,7 @@ def _check_schedule(seq_lens, s_q, units, max_pages=None):
     load = np.zeros(units, dtype=np.int64)
     for (row, j0, j1, part), u in zip(items.tolist(), unit.tolist()):
         load[u] += (j1 - j0 + 63) // 64 + item_cost
-    bound = h["target"] + 2 * (MIN_SPLIT + item_cost)
+    bound = h["target"] + 2 * (min_split + item_cost)
     assert load.max() <= bound, (load.max(), h["target"])
     return r, load
 
