@@ -125,6 +125,7 @@ mla_status mla_decode_plan_host(const mla_problem *prob, const int32_t *seq_lens
 
 mla_status mla_decode_plan(const mla_problem *prob, const int32_t *seq_lens, void *workspace,
                            size_t workspace_bytes, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_decode_plan");
     mla_status st = check_problem(prob);
     if (st != MLA_OK) return st;
     if (!seq_lens || !aligned16(seq_lens) || !workspace || !aligned16(workspace))
@@ -182,6 +183,7 @@ mla_status mla_decode(const mla_problem *prob, const void *q_latent, const void 
                       const void *kv_cache, int64_t num_pages, const int32_t *block_table,
                       float scale, void *o_latent, float *lse, void *workspace,
                       size_t workspace_bytes, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_decode");
     return decode_impl(prob, q_latent, q_rope, kv_cache, num_pages, block_table, scale, o_latent,
                        lse, workspace, workspace_bytes, stream, nullptr);
 }
@@ -190,6 +192,7 @@ mla_status mla_decode_timed(const mla_problem *prob, const void *q_latent, const
                             const void *kv_cache, int64_t num_pages, const int32_t *block_table,
                             float scale, void *o_latent, float *lse, void *workspace,
                             size_t workspace_bytes, mla_stream_t stream, void *const *events) {
+    mla::NvtxRange nvtx_range("mla_decode_timed");
     return decode_impl(prob, q_latent, q_rope, kv_cache, num_pages, block_table, scale, o_latent,
                        lse, workspace, workspace_bytes, stream, events);
 }
@@ -199,6 +202,7 @@ mla_status mla_decode_diag(const mla_problem *prob, const void *q_latent, const 
                            float scale, void *o_latent, float *lse, void *workspace,
                            size_t workspace_bytes, mla_stream_t stream, uint64_t wait_limit_ns,
                            uint32_t inject) {
+    mla::NvtxRange nvtx_range("mla_decode_diag");
     if (wait_limit_ns < 1000ull || wait_limit_ns > 60000000000ull) return MLA_ERR_INVALID_ARG;
     if (inject & ~MLA_INJECT_WITHHOLD_K_LOAD) return MLA_ERR_INVALID_ARG;
     return decode_impl(prob, q_latent, q_rope, kv_cache, num_pages, block_table, scale, o_latent,
@@ -209,6 +213,7 @@ mla_status mla_decode_fp8(const mla_problem *prob, const void *q_latent, const v
                           const void *kv_cache_fp8, int64_t num_pages, const int32_t *block_table,
                           float scale, void *o_latent, float *lse, void *workspace,
                           size_t workspace_bytes, mla_stream_t stream, void *const *events) {
+    mla::NvtxRange nvtx_range("mla_decode_fp8");
     return decode_impl(prob, q_latent, q_rope, kv_cache_fp8, num_pages, block_table, scale, o_latent,
                        lse, workspace, workspace_bytes, stream, events, mla::kDefaultWaitLimitNs, 0, true);
 }

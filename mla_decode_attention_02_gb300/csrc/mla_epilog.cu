@@ -223,6 +223,7 @@ bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 
 extern "C" mla_status mla_epilog_uv(const mla_problem *prob, const void *o_latent, const void *w_uv,
                                     void *o_v, int32_t *device_status, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_epilog_uv");
     using namespace mla;
     if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->flags != 0)
         return MLA_ERR_INVALID_ARG;

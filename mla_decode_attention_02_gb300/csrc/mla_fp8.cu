@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) mla_quantize_fp8_kernel(cons
 
 extern "C" mla_status mla_cache_quantize_fp8(const void *kv_cache, int64_t num_rows, void *kv_cache_fp8,
                                              mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_cache_quantize_fp8");
     using namespace mla;
     if (!kv_cache || !kv_cache_fp8 || num_rows < 1 || (reinterpret_cast<uintptr_t>(kv_cache) & 15u) ||
         (reinterpret_cast<uintptr_t>(kv_cache_fp8) & 15u))

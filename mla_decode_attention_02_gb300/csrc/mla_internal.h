@@ -7,6 +7,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "mla_decode.h"
 
 #if defined(__CUDACC__)
@@ -16,6 +18,16 @@
 #endif
 
 namespace mla {
+
+// An NVTX range over a C-ABI call (the host-side enqueue of its launches), for
+// timelines of profiling tools; with no tool attached push and pop return at
+// once (NVTX v3 is header-only and loads nothing by itself).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr int kHeads = MLA_NUM_HEADS;    // query heads sharing one latent row
 constexpr int kDl = MLA_D_LATENT;        // c_kv values per cached row (also V)

@@ -46,6 +46,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_problem *prob, const void *q_
                                          int64_t num_pages, const int32_t *block_table,
                                          const int32_t *seq_lens, float scale, void *o_latent,
                                          float *lse, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_decode_noalloc");
     // Every argument is checked before anything is enqueued: the planner below
     // would otherwise run (and rewrite the shared array) for a call that
     // mla_decode then refuses.

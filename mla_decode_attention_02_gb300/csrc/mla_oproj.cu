@@ -272,6 +272,7 @@ bool g_attr[64];
 
 extern "C" mla_status mla_epilog_oproj(int32_t tokens, int32_t hidden, const void *o_v, const void *w_o,
                                        void *out, int32_t *device_status, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_epilog_oproj");
     using namespace mla;
     auto aligned16 = [](const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (tokens < 1 || hidden < 8 || hidden % 8 != 0 || !aligned16(o_v) || !aligned16(w_o) || !aligned16(out) ||

@@ -394,6 +394,7 @@ extern "C" mla_status mla_prolog(const mla_problem *prob, const void *q_nope, co
                                  void *kv_cache, int64_t num_pages, const int32_t *block_table,
                                  const int32_t *seq_lens, void *q_latent, void *q_rope,
                                  int32_t *device_status, mla_stream_t stream) {
+    mla::NvtxRange nvtx_range("mla_prolog");
     using namespace mla;
     if (!prob || prob->batch < 1 || prob->max_pages_per_seq < 1 || prob->flags != 0)
         return MLA_ERR_INVALID_ARG;
