@@ -27,6 +27,12 @@ constexpr int kCombineWarps = 8;
 constexpr int kCombineGrid = 1024;  // CTAs; warps stride over (row, head) tasks
 
 constexpr int kWarpParts = 8;      // rows with more parts are merged by a whole CTA per head
+// Parts whose rows are loaded before any of them is summed.  Two, with the
+// kernel held to 80 registers (three CTAs per SM): MTP's merge 16.2 -> 14.4 us,
+// long-1M's 13.4 -> 12.0 us; four needs 141 registers, and the lost occupancy
+// made mixed and MTP slower.
+constexpr int kBatch = 2;
+static_assert(kWarpParts <= 32, "one part's lse per lane");
 
 // o = acc / W -> bf16 (lane owns four float4 columns of the 512), lse = M + ln W.
 __device__ __forceinline__ void store_row(__nv_bfloat16 *orow, float *lse, const float4 (&acc)[4], float W,
@@ -70,18 +76,36 @@ __device__ __forceinline__ void merge_task_cta(int32_t r, int32_t h, int32_t n, 
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float W = 0.f;
-    for (int32_t i = warp; i < n; i += kCombineWarps) {
-        const size_t slot = (size_t)(part0 + i) * kHeads + h;
-        const float w = expf(lse_part[slot] - M);
-        W += w;
-        const float4 *src = reinterpret_cast<const float4 *>(o_part + slot * kDl);
+    // this warp's parts (warp, warp + 8, ...) in order, kBatch at a time: every
+    // load of a batch is in flight before the first is summed
+#pragma unroll 1
+    for (int32_t i0 = warp; i0 < n; i0 += kBatch * kCombineWarps) {
+        float lse_j[kBatch];
+        float4 v[kBatch][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 v = src[k * 32 + lane];
-            acc[k].x += w * v.x;
-            acc[k].y += w * v.y;
-            acc[k].z += w * v.z;
-            acc[k].w += w * v.w;
+        for (int j = 0; j < kBatch; ++j) {
+            const int32_t i = i0 + j * kCombineWarps;
+            if (i < n) {
+                const size_t slot = (size_t)(part0 + i) * kHeads + h;
+                lse_j[j] = lse_part[slot];
+                const float4 *src = reinterpret_cast<const float4 *>(o_part + slot * kDl);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[j][k] = src[k * 32 + lane];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (i0 + j * kCombineWarps < n) {
+                const float w = expf(lse_j[j] - M);
+                W += w;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[k].x += w * v[j][k].x;
+                    acc[k].y += w * v[j][k].y;
+                    acc[k].z += w * v[j][k].z;
+                    acc[k].w += w * v[j][k].w;
+                }
+            }
         }
     }
 #pragma unroll
@@ -111,7 +135,7 @@ __device__ __forceinline__ void merge_task_cta(int32_t r, int32_t h, int32_t n, 
     __syncthreads();   // red / red_m are reused by the next task
 }
 
-__global__ void __launch_bounds__(32 * kCombineWarps)
+__global__ void __launch_bounds__(32 * kCombineWarps, 3)
 mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o_latent,
                    float *__restrict__ lse_out, int32_t batch, int32_t s_q, int32_t num_units) {
     __shared__ float4 red[kCombineWarps][4][32];   // per warp: its lanes' 16 partial sums
@@ -146,26 +170,43 @@ mla_combine_kernel(const uint8_t *__restrict__ ws, __nv_bfloat16 *__restrict__ o
             continue;
         }
         const int32_t part0 = row_part0[r];
-        float M = -INFINITY;
-        for (int32_t i = lane; i < n; i += 32) M = fmaxf(M, lse_part[(size_t)(part0 + i) * kHeads + h]);
+        // lane i < n holds part i's lse and weight
+        const float lse_i = lane < n ? lse_part[(size_t)(part0 + lane) * kHeads + h] : -INFINITY;
+        float M = lse_i;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w_i = lane < n ? expf(lse_i - M) : 0.f;
         float4 acc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         float W = 0.f;
-        for (int32_t i = 0; i < n; ++i) {
-            const size_t slot = (size_t)(part0 + i) * kHeads + h;
-            const float w = expf(lse_part[slot] - M);
-            W += w;
-            const float4 *src = reinterpret_cast<const float4 *>(o_part + slot * kDl);
+        // the parts in index order, kBatch at a time: every load of a batch is in
+        // flight before the first is summed
+#pragma unroll 1
+        for (int32_t i0 = 0; i0 < n; i0 += kBatch) {
+            float4 v[kBatch][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = src[k * 32 + lane];
-                acc[k].x += w * v.x;
-                acc[k].y += w * v.y;
-                acc[k].z += w * v.z;
-                acc[k].w += w * v.w;
+            for (int j = 0; j < kBatch; ++j) {
+                if (i0 + j < n) {
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(o_part + ((size_t)(part0 + i0 + j) * kHeads + h) * kDl);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v[j][k] = src[k * 32 + lane];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_i, (i0 + j) & 31);
+                if (i0 + j < n) {
+                    W += w;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[k].x += w * v[j][k].x;
+                        acc[k].y += w * v[j][k].y;
+                        acc[k].z += w * v[j][k].z;
+                        acc[k].w += w * v[j][k].w;
+                    }
+                }
             }
         }
         store_row(orow, lse_out + (size_t)r * kHeads + h, acc, W, M, lane);
