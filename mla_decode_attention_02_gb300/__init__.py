@@ -18,6 +18,11 @@ and the step after it (``include/mla_epilog.h``) projects the heads back out:
 
     o_v, st = epilog_uv(o_latent, w_uv)                      # mla_epilog_uv
     out = epilog_oproj(o_v, w_o)                             # mla_epilog_oproj
+
+An fp8 (e4m3) cache (``include/mla_fp8.h``) holds half the bytes per token:
+
+    kv8 = quantize_cache_fp8(kv_cache)                       # mla_cache_quantize_fp8
+    o_latent, lse = decode_fp8(p, q_latent, q_rope, kv8, block_table)   # mla_decode_fp8
 """
 
 from ._binding import (D_V, HIDDEN, DEFAULT_ROPE_BASE, DEFAULT_RMS_EPS, DEFAULT_SCALE, D_LATENT, D_NOPE, D_ROPE, LIB_PATH, NUM_HEADS, PAGE_SIZE,
