@@ -33,8 +33,10 @@ def _within(gpu, ref, absdot, k, what):
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the bound, worst err {err.max():.3e}"
 
 
-@pytest.mark.parametrize("batch,s_q", [(1, 1), (64, 1), (65, 2), (128, 2), (3, 2)])
+@pytest.mark.parametrize("batch,s_q", [(1, 1), (64, 1), (65, 2), (128, 2), (3, 2), (129, 1), (150, 2)])
 def test_uv_parity(batch, s_q):
+    """Token counts below, at and above one 128-token tile, ragged last tiles included
+    (129 tokens: a one-token tile; 300 tokens: three tiles)."""
     T = batch * s_q
     e = W.epilog_tensors(T, seed=T)
     o_lat = e["o_latent"].view(batch, s_q, 128, 512).cuda()
