@@ -325,7 +325,7 @@ def _config(w):
 
 
 PER_WORKLOADS = ("mixed", "mtp", "long", "long1m", "uniform+pow2", "mixed+pow2", "uniform+fp8",
-                 "mixed+fp8")
+                 "mixed+fp8", "long+fp8")
 STEP_KERNELS = 3          # launches per step: planner, main kernel, merge
 
 
