@@ -170,7 +170,7 @@ enum : uint32_t {
     B_OFREE = B_PVLAST + 1,              // epilogue done reading O
     B_EPI = B_OFREE + 1,                 // merge warps done with the staged epilogue
     B_DRAIN = B_EPI + 1,                 // + issuer (0: score, 1: PV)
-    B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-255 staged (+tx)
+    B_QSTAGE = B_DRAIN + 2,              // item start: q dims 0-319 staged (+tx)
     B_QCOPIED = B_QSTAGE + 1,            // item start: softmax warps moved the staged q to TMEM
     B_QTILE = B_QCOPIED + 1,             // q dims 384-575 landed in the shared-memory q tile (+tx)
     B_KCONV = B_QTILE + 1,               // fp8: + page parity: K stage converted to bf16
@@ -652,7 +652,7 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
                         if (k0 + kk == 0) {
                             // Item start: this CTA's score MMAs of the previous item are
                             // done, so the K stage of this item's second page and the
-                            // shared-memory q tile are free.  Stage q dims 0-255 there
+                            // shared-memory q tile are free.  Stage q dims 0-319 there
                             // (see q_stage_off) beside this page's K load; this item's
                             // q dims 384-575 follow once the softmax warps moved the
                             // staged blocks into TMEM.
@@ -880,9 +880,10 @@ mla_main_tc_kernel(const __grid_constant__ Params P) {
             const int valid_last = it.kv_end - (it.kv_begin + (n - 1) * kPage);
             const uint32_t ii = (uint32_t)(i - i_begin);
 
-            // q of this head -> TMEM: dims 0-255 from the staged blocks (the
+            // q of this head -> TMEM: dims 0-319 from the staged blocks (the
             // staging was issued after the previous item's score MMAs were done, into
-            // the K stage of the item's second page), dims 256-383 through registers
+            // the K stage of the item's second page and the q tile), dims 320-383
+            // through registers
             {
                 constexpr int kRegChunks = kQTDims / 64 - kQStaged;
                 const uint4 *src = reinterpret_cast<const uint4 *>(P.q_latent + ((size_t)it.row * kHeads + h) * kDl) +
