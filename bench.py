@@ -67,6 +67,9 @@ def _args():
                          "power-of-two maxima) of the decode stage")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of from one captured CUDA graph")
+    ap.add_argument("--cache", choices=["bf16", "fp8"], default="bf16",
+                    help="decode stage: the latent cache's format (fp8: e4m3 rows of 656 bytes, "
+                         "quantised by the library before the timed region; 656 algorithmic bytes per key)")
     return ap.parse_args()
 
 
@@ -238,16 +241,37 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _cpu_baseline(w, inp, budget_s: float = 15.0):
-    """The oracle as it stands, on this host's cores, over a bounded sample of the workload."""
+def _cpu_baseline(w, inp, budget_s: float = 15.0, fp8: bool = False):
+    """The oracle as it stands, on this host's cores, over a bounded sample of the workload.
+
+    With fp8, the oracle's fp8 decode (attention of the dequantised rows) over the sampled
+    requests' pages, quantised by the oracle's own quantiser outside the timed part.
+    """
+    import torch
     import oracle
+    from oracle import fp8 as OF
     threads = oracle.default_threads()
 
     def run(reqs):
         rows = [(b, t, h) for b in reqs for t in range(w.s_q) for h in range(W.NUM_HEADS)]
+        if not fp8:
+            t0 = time.perf_counter()
+            oracle.decode(inp["q_latent"], inp["q_rope"], inp["kv_cache"], inp["block_table"],
+                          inp["seq_lens"], s_q=w.s_q, scale=inp["scale"], rows=rows, threads=threads)
+            return time.perf_counter() - t0
+        # the sampled requests' pages only, renumbered
+        pages = sorted({int(p) for b in reqs
+                        for p in inp["block_table"][b, :(w.seq_lens[b] + W.PAGE - 1) // W.PAGE].tolist()})
+        remap = {p: i for i, p in enumerate(pages)}
+        bt = torch.full_like(inp["block_table"], -1)
+        for b in reqs:
+            n = (w.seq_lens[b] + W.PAGE - 1) // W.PAGE
+            bt[b, :n] = torch.tensor([remap[int(p)] for p in inp["block_table"][b, :n].tolist()],
+                                     dtype=torch.int32)
+        q8 = OF.quantize_cache(inp["kv_cache"][torch.tensor(pages, dtype=torch.long)])
         t0 = time.perf_counter()
-        oracle.decode(inp["q_latent"], inp["q_rope"], inp["kv_cache"], inp["block_table"],
-                      inp["seq_lens"], s_q=w.s_q, scale=inp["scale"], rows=rows, threads=threads)
+        OF.decode(inp["q_latent"], inp["q_rope"], q8, bt, inp["seq_lens"], s_q=w.s_q, scale=inp["scale"],
+                  rows=rows, threads=threads)
         return time.perf_counter() - t0
 
     order = sorted(range(w.batch), key=lambda b: w.seq_lens[b])
@@ -261,10 +285,11 @@ def _cpu_baseline(w, inp, budget_s: float = 15.0):
         reqs.append(b)
         keys += w.seq_lens[b]
     dt = run(reqs)
-    nbytes = W.cache_bytes([w.seq_lens[b] for b in reqs])
+    sample_lens = [w.seq_lens[b] for b in reqs]
+    nbytes = W.cache_bytes_fp8(sample_lens) if fp8 else W.cache_bytes(sample_lens)
     return {"value": nbytes / dt / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(reqs)} of {w.batch} requests (all {W.NUM_HEADS} heads, "
-                      f"{keys} keys), {dt:.1f} s wall, fp64"}
+                      f"{keys} keys{', fp8 cache' if fp8 else ''}), {dt:.1f} s wall, fp64"}
 
 
 def run_reference(args, rank, world):
@@ -313,7 +338,7 @@ def run_reference(args, rank, world):
     return 0
 
 
-def _config(w):
+def _config(w, fp8: bool = False):
     lens = sorted(set(w.seq_lens))
     desc = (f"{w.batch}x{lens[0]}" if len(lens) == 1 else
             f"{len(w.seq_lens)} rows, seq_len {min(lens)}..{max(lens)}")
@@ -321,7 +346,7 @@ def _config(w):
             "d_latent": W.D_LATENT, "d_rope": W.D_ROPE, "page": W.PAGE, "seq_lens": desc,
             "total_keys": sum(w.seq_lens),
             "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write); "
-                  f"cache {W.cache_bytes(w.seq_lens) / 1e6:.0f} MB"}
+                  f"cache {(W.cache_bytes_fp8 if fp8 else W.cache_bytes)(w.seq_lens) / 1e6:.0f} MB"}
 
 
 PER_WORKLOADS = ("mixed", "mtp", "long", "long1m", "uniform+pow2", "mixed+pow2", "uniform+fp8",
@@ -498,9 +523,10 @@ def run_native(args, rank, world, local):
     peaks, peak_src = _peaks()
 
     w = W.workload(args.workload)
+    fp8 = args.cache == "fp8"
     min_steps = args.steps if args.steps is not None else 20
     m = _measure(w, dev, world, min_steps, 1.5, not args.no_graph, args.warmup,
-                 sampler_gpu=gpu_id if rank == 0 else False)
+                 sampler_gpu=gpu_id if rank == 0 else False, fp8=fp8)
     step_ms, main_ms = m["step_ms"], m["main_ms"]
     steps = m["steps"]
     m_plan_us, m_comb_us, m_phase_us = m["plan_ms"] * 1e3, m["comb_ms"] * 1e3, m["phase_step_ms"] * 1e3
@@ -510,7 +536,7 @@ def run_native(args, rank, world, local):
     stream = torch.cuda.current_stream()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    cache_b = W.cache_bytes(w.seq_lens)
+    cache_b = W.cache_bytes_fp8(w.seq_lens) if fp8 else W.cache_bytes(w.seq_lens)
     fl = W.flops(w.seq_lens, S)
     value = whole_job_tbs(world, cache_b, step_ms)
 
@@ -553,8 +579,9 @@ def run_native(args, rank, world, local):
                         s_comp.wait_event(out_done[k - 2])   # step k - 2's results are copied out
                     flush.fill_(k & 0xFF)
                     p = mla.plan(dbuf[b]["seq_lens"], s_q=S, max_pages_per_seq=mp, workspace=ws)
-                    mla.decode(p, dbuf[b]["q_latent"], dbuf[b]["q_rope"], d["kv_cache"],
-                               dbuf[b]["block_table"], scale=d["scale"], out=outs[b][0], lse=outs[b][1])
+                    dec = mla.decode_fp8 if fp8 else mla.decode
+                    dec(p, dbuf[b]["q_latent"], dbuf[b]["q_rope"], d["kv8"] if fp8 else d["kv_cache"],
+                        dbuf[b]["block_table"], scale=d["scale"], out=outs[b][0], lse=outs[b][1])
                     comp_done[k] = torch.cuda.Event()
                     comp_done[k].record(s_comp)
                 with torch.cuda.stream(s_out):
@@ -593,7 +620,7 @@ def run_native(args, rank, world, local):
                        "elapsed time of the whole loop, L2 flush before every step included; the "
                        "KV cache is device-resident serving state"}
 
-    roof = _roofline(w, main_ms, peaks, peak_src, _ncu_traffic(w.name))
+    roof = _roofline(w, main_ms, peaks, peak_src, None if fp8 else _ncu_traffic(w.name), fp8=fp8)
     t_roof = max(cache_b / (NOMINAL_HBM_TBS * 1e12), fl / (peaks["bf16_tflops"] * 1e12))
     t_roof_meas = max(cache_b / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
     del m, d, out, lse, ws, flush
@@ -605,7 +632,7 @@ def run_native(args, rank, world, local):
             # "<workload>+pow2": the same workload with power-of-two running maxima;
             # "<workload>+fp8": the same workload over the fp8 cache
             base, _, mode = name.partition("+")
-            if name == w.name:
+            if base == w.name and mode == ("fp8" if fp8 else ""):
                 continue
             wk = W.workload(base)
             r = _measure(wk, dev, world, 20, 0.3, not args.no_graph, 3, sampler_gpu=False,
@@ -614,7 +641,7 @@ def run_native(args, rank, world, local):
                            fp8=mode == "fp8")
             kb = W.cache_bytes_fp8(wk.seq_lens) if mode == "fp8" else W.cache_bytes(wk.seq_lens)
             per_workload[name] = {
-                "config": _config(wk), "steps": r["steps"], "us_per_step": r["step_ms"] * 1e3,
+                "config": _config(wk, mode == "fp8"), "steps": r["steps"], "us_per_step": r["step_ms"] * 1e3,
                 "tb_s_step": whole_job_tbs(world, kb, r["step_ms"]),
                 "phases_us": {"plan": r["plan_ms"] * 1e3, "main": r["main_ms"] * 1e3,
                               "combine": r["comb_ms"] * 1e3},
@@ -628,13 +655,13 @@ def run_native(args, rank, world, local):
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu_base = _cpu_baseline(w, cpu)
+        cpu_base = _cpu_baseline(w, cpu, fp8=fp8)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
                 "steps": steps, "warmup": args.warmup, "ms_per_step": step_ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic", "config": _config(w),
+                "data": "synthetic", "config": {**_config(w, fp8), "cache": args.cache},
                 "tflops": world * fl / (step_ms * 1e-3) / 1e12,
                 "us_per_step": step_ms * 1e3,
                 "phases_us": {"plan": m_plan_us, "main": main_ms * 1e3, "combine": m_comb_us,
